@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Throughput of the nanochat-style pretraining step (forward + backward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20_bf16]
+    python bench.py --impl reference ...     # the fp64 CPU oracle on host cores
+
+One step = nc_step over one batch: embedding + norm, every block forward,
+LM head + softcap + cross-entropy with its backward, every block backward,
+embedding backward -- all weight gradients produced.  Inputs are synthetic
+(Zipf(1.1) token ids, N(0, 1/fan_in) bf16 weights) and resident in HBM when
+the timed region starts.  The working set (~40 GB at d20) is far larger than
+the 126 MB L2, so no flush is needed between steps.
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own batch of the
+same shape: the step shards by batch rows with no data-path collective, so
+scaling is weak; the only collectives are the timing barrier and the max
+over ranks.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import nc_synth  # noqa: E402
+from pretraining_step_pretrain_b300 import flops  # noqa: E402
+
+METRIC = "train tokens/sec (fwd+bwd) at d20 shape, 1×B300; MFU vs bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- roofline
+def algorithmic_cost(name, shape, B, T):
+    """(kind, amount) per launch of a named launch group: FLOPs for tensor-core
+    work, bytes for memory-bound work (minimum HBM traffic of the operation)."""
+    d, H, h, f, V = shape.d_model, shape.n_head, shape.head_dim, shape.d_mlp, shape.vocab
+    M, q = B * T, (H + 2) * h
+    gemm = {"qkv": 2 * M * d * q, "out": 2 * M * H * h * d, "fc": 2 * M * d * f,
+            "proj": 2 * M * f * d}
+    causal_matmul = B * H * T * T * h          # one causal-half matmul (2 * T^2/2 * h)
+    if name.startswith("fwd.") and name.endswith("_gemm"):
+        return "tensor", gemm[name[4:-5]]
+    if name.startswith("bwd.") and name.endswith("_gemm"):
+        return "tensor", gemm[name[4:].split("_")[0]]
+    if name in ("lm.logits_gemm", "lm.dw_gemm", "lm.dx_gemm"):
+        return "tensor", 2 * M * d * V
+    if name == "fwd.attention":
+        return "tensor", 2 * causal_matmul
+    if name == "bwd.attention":
+        return "tensor", 5 * causal_matmul
+    if name in ("fwd.norm1", "fwd.norm2", "lm.norm"):
+        return "hbm", M * d * (4 + 2) + M * 4
+    if name in ("bwd.norm1_bwd", "bwd.norm2_bwd", "lm.norm_bwd"):
+        return "hbm", M * d * (2 + 2 + 4 + 4 + 2)
+    if name == "fwd.qknorm_rope":
+        return "hbm", M * q * 2 * 2
+    if name == "bwd.qknorm_rope":
+        return "hbm", M * (H + 1) * h * 2 * 3
+    if name == "lm.dlogits":
+        return "hbm", M * V * 2 * 2
+    if name == "embed.norm":
+        return "hbm", M * d * (2 + 4)
+    if name == "embed_bwd":
+        return "hbm", M * d * (4 + 2 + 4 + 4) + V * d * 4
+    return None, 0
+
+
+def profile_kernels(st, steps, shape, B, T):
+    from pretraining_step_pretrain_b300 import nc
+    import torch
+    nc.profile_start(200 * (shape.depth + 2) * steps)
+    for _ in range(steps):
+        st.run()
+    torch.cuda.synchronize()
+    recs = nc.profile_stop()
+    agg = {}
+    for name, ms in recs:
+        a = agg.setdefault(name, [0.0, 0])
+        a[0] += ms
+        a[1] += 1
+    total = sum(v[0] for v in agg.values())
+    rows = sorted(agg.items(), key=lambda kv: -kv[1][0])
+    return rows, total
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(shape, T, min_seconds, max_steps, weights=None):
+    """Time the fp64 oracle on one row of T tokens at `shape` (host cores)."""
+    import oracle
+    from threadpoolctl import threadpool_info
+    if weights is None:
+        weights = nc_synth.make_weights(shape, seed=1, bf16=True)
+    P = {k: v.astype(np.float64) for k, v in weights.items()}
+    ids, tg = nc_synth.make_tokens(shape.vocab, 1, T, seed=0)
+    oracle.step(shape, P, ids, tg)                       # first touch of every buffer
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and (time.perf_counter() - t_all < min_seconds or not times):
+        t0 = time.perf_counter()
+        oracle.step(shape, P, ids, tg)
+        times.append(time.perf_counter() - t0)
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    return T * len(times) / sum(times), threads, len(times)
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = nc_synth.WORKLOADS[args.workload]
+    shape = w.shape
+    T = args.ref_tokens
+    weights = nc_synth.make_weights(shape, seed=1, bf16=True)
+    import oracle
+    from threadpoolctl import threadpool_info
+    P = {k: v.astype(np.float64) for k, v in weights.items()}
+    ids, tg = nc_synth.make_tokens(shape.vocab, 1, T, seed=0)
+    for _ in range(args.warmup):
+        oracle.step(shape, P, ids, tg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.step(shape, P, ids, tg)
+    dt = time.perf_counter() - t0
+    value = T * args.steps / dt
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    sample = f"{w.name} widths, 1 row x {T} tokens per step (fp64 numpy oracle)"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": config_dict(w, args.gpus),
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def config_dict(w, n):
+    return {"workload": w.name, "depth": w.shape.depth, "d_model": w.shape.d_model,
+            "n_head": w.shape.n_head, "head_dim": w.shape.head_dim, "n_kv_head": 1,
+            "d_mlp": w.shape.d_mlp, "vocab": w.shape.vocab, "batch_per_gpu": w.batch,
+            "global_batch": w.batch * n, "seq_len": w.seq,
+            "parallelism": f"batch rows sharded over {n} GPU(s), no collective",
+            "l2": "no flush: working set far larger than L2"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from pretraining_step_pretrain_b300 import nc
+    torch.cuda.set_device(local_rank)
+    w = nc_synth.WORKLOADS[args.workload]
+    shape, B, T = w.shape, w.batch, w.seq
+    weights = nc_synth.make_weights(shape, seed=1, bf16=(w.dtype == "bf16"))
+    ids, tg = nc_synth.make_tokens(shape.vocab, B, T, seed=rank, dist=w.ids)
+    st = nc.Step(shape, w.dtype, B, T, weights, device=f"cuda:{local_rank}")
+    ids_d = torch.from_numpy(ids).cuda()
+    tg_d = torch.from_numpy(tg).cuda()
+    st.ids.copy_(ids_d)
+    st.targets.copy_(tg_d)
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    if st.status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v]
+    gpu_idx = local_rank
+    if local_rank < len(visible) and visible[local_rank].isdigit():
+        gpu_idx = int(visible[local_rank])
+    clocks = ClockSampler(gpu_idx)
+    barrier()
+    clocks.start()
+    n0 = nc.launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = nc.launch_count() - n0
+    clk = clocks.stop()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if st.status() != 0:
+        raise RuntimeError("device error during the timed steps")
+    loss = float(st.loss.item())
+    tokens = B * T * world * args.steps
+    value = tokens / (ms / 1000.0)
+
+    # end to end through the public call with host buffers
+    ids_h = torch.from_numpy(ids).pin_memory()
+    tg_h = torch.from_numpy(tg).pin_memory()
+    st.run_host(ids_h, tg_h)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.run_host(ids_h, tg_h)
+    t_e2e = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    e2e = {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
+           "d2h_bytes_per_step": 4}
+
+    # per-kernel attribution (separate, profiled steps)
+    rows, prof_total = profile_kernels(st, args.profile_steps, shape, B, T)
+    peaks, peak_src = load_peaks()
+    top = None
+    for name, (tot, cnt) in rows:
+        kind, amount = algorithmic_cost(name, shape, B, T)
+        if kind is not None:
+            top = (name, tot, cnt, kind, amount)
+            break
+    roofline = None
+    if top:
+        name, tot, cnt, kind, amount = top
+        per_launch_s = tot / cnt / 1000.0
+        if kind == "tensor":
+            achieved = amount / per_launch_s / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roofline = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
+                        "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                        "peak_source": f"{peak_src} bf16 sustained", "share": tot / prof_total,
+                        "algorithmic_per_launch": amount}
+        else:
+            achieved = amount / per_launch_s / 1e9
+            peak = peaks["hbm_gbs"]
+            roofline = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": peak,
+                        "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                        "peak_source": f"{peak_src} copy bandwidth", "share": tot / prof_total,
+                        "algorithmic_per_launch": amount}
+    kernels = []
+    for name, (tot, cnt) in rows[:12]:
+        kind, amount = algorithmic_cost(name, shape, B, T)
+        entry = {"name": name, "ms_per_step": tot / args.profile_steps,
+                 "share": tot / prof_total}
+        if kind == "tensor":
+            entry["tflops"] = amount * cnt / (tot / 1000.0) / 1e12
+        elif kind == "hbm":
+            entry["gbs"] = amount * cnt / (tot / 1000.0) / 1e9
+        kernels.append(entry)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del st
+        torch.cuda.empty_cache()
+        v, threads, n = oracle_tokens_per_s(shape, args.cpu_tokens, 10.0, 3, weights)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{w.name} widths, 1 row x {args.cpu_tokens} tokens, {n} timed "
+                         f"oracle step(s) after one untimed"}
+
+    f_tok = flops.flops_per_token(shape, T)
+    f_tok_causal = flops.flops_per_token(shape, T, causal_actual=True)
+    per_gpu = value / world
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": w.dtype, "data": "synthetic: Zipf(1.1) token ids, N(0,1/fan_in) weights",
+           "config": config_dict(w, world),
+           "mfu": per_gpu * f_tok / (peaks["bf16_tflops"] * 1e12),
+           "mfu_detail": {"flops_per_token_palm": f_tok, "flops_per_token_causal": f_tok_causal,
+                          "vs_measured_burst": per_gpu * f_tok / (peaks["bf16_tflops"] * 1e12),
+                          "vs_measured_sustained":
+                              per_gpu * f_tok / (peaks["bf16_tflops_sustained"] * 1e12),
+                          "vs_nominal_2250": per_gpu * f_tok / (NOMINAL_BF16_TFLOPS * 1e12),
+                          "causal_actual_vs_measured_burst":
+                              per_gpu * f_tok_causal / (peaks["bf16_tflops"] * 1e12),
+                          "peak_source": peak_src},
+           "loss": loss, "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
+           "e2e": e2e, "gpu_launches": launches, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="d20_bf16", choices=sorted(nc_synth.WORKLOADS))
+    ap.add_argument("--profile-steps", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -88,13 +88,9 @@ def make_tokens(vocab: int, batch: int, seq: int, seed: int = 0,
 
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bfloat16 (ties to even), kept as float32."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    nan = np.isnan(a)
-    out = rounded.astype(np.uint32).view(np.float32).copy()
-    out[nan] = np.nan
-    return out
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float32).numpy()
 
 
 def weight_shapes(shape: ModelShape) -> dict[str, tuple[int, int]]:

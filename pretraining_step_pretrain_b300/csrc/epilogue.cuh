@@ -1,0 +1,164 @@
+// GEMM epilogues shared by the tcgen05 kernel (bf16) and the SIMT kernel (fp32).
+//
+// Each epilogue receives W consecutive fp32 accumulators of one output row,
+// starting at column `col` (W = 32 in the tensor-core kernel, W = 4 in the
+// SIMT kernel), and returns a per-chunk contribution to a row reduction that
+// only the softcap/cross-entropy epilogue uses.  The caller guarantees
+// row < M and col + W <= N.
+#pragma once
+
+#include "nc_common.cuh"
+
+namespace nc {
+
+template <typename T, int W>
+__device__ __forceinline__ void store_row_chunk(T* p, const float (&v)[W]) {
+#pragma unroll
+  for (int i = 0; i < W; i += 4) {
+    float t[4] = {v[i], v[i + 1], v[i + 2], v[i + 3]};
+    Vec4<T>::store(p + i, t);
+  }
+}
+template <typename T, int W>
+__device__ __forceinline__ void load_row_chunk(const T* p, float (&v)[W]) {
+#pragma unroll
+  for (int i = 0; i < W; i += 4) {
+    float t[4];
+    Vec4<T>::load(p + i, t);
+    v[i] = t[0]; v[i + 1] = t[1]; v[i + 2] = t[2]; v[i + 3] = t[3];
+  }
+}
+
+// C = acc (activation type: bf16 or fp32).
+template <typename TOut>
+struct EpiStore {
+  static constexpr bool kRowReduce = false;
+  TOut* c;
+  long ldc;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+    store_row_chunk<TOut, W>(c + (long)row * ldc + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
+// Float32 store for weight gradients.  With split-K each split writes its own
+// slab (c + split * split_stride) and a reduction kernel sums the slabs in a
+// fixed order; with one split the epilogue writes (or accumulates into) C.
+struct EpiStoreF32 {
+  static constexpr bool kRowReduce = false;
+  float* c;
+  long ldc;
+  long split_stride;
+  int accumulate;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int split) const {
+    float* p = c + split * split_stride + (long)row * ldc + col;
+    if (accumulate) {
+      float o[W];
+      load_row_chunk<float, W>(p, o);
+#pragma unroll
+      for (int i = 0; i < W; ++i) v[i] += o[i];
+    }
+    store_row_chunk<float, W>(p, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
+// Residual add into the float32 stream: X += acc.
+struct EpiAddF32 {
+  static constexpr bool kRowReduce = false;
+  float* x;
+  long ldx;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+    float* p = x + (long)row * ldx + col;
+    float o[W];
+    load_row_chunk<float, W>(p, o);
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] += o[i];
+    store_row_chunk<float, W>(p, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
+// ReLU^2 MLP activation: a = max(u, 0)^2.  Only `a` is kept: backward needs
+// relu(u) = sqrt(a), which is recovered from `a` (see EpiRelu2Bwd).
+template <typename TOut>
+struct EpiRelu2 {
+  static constexpr bool kRowReduce = false;
+  TOut* a;
+  long lda;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      float r = fmaxf(v[i], 0.f);
+      v[i] = r * r;
+    }
+    store_row_chunk<TOut, W>(a + (long)row * lda + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
+// Backward of ReLU^2 fused after dA = dY Wproj: dU = dA * 2 relu(u), with
+// relu(u) = sqrt(a) read from the saved activation a = relu(u)^2.
+template <typename TOut>
+struct EpiRelu2Bwd {
+  static constexpr bool kRowReduce = false;
+  TOut* du;
+  const TOut* a;
+  long ld;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+    float av[W];
+    load_row_chunk<TOut, W>(a + (long)row * ld + col, av);
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] *= 2.f * sqrtf(av[i]);
+    store_row_chunk<TOut, W>(du + (long)row * ld + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
+// LM head epilogue (tensor-core path): s = c tanh(z / c) stored as fp16 --
+// |s| <= c = 15 lies well inside fp16's range and fp16 keeps 3 more mantissa
+// bits than bf16 there; the per-row sum of exp(s) over this tile's columns
+// goes to part[row * n_part + col_tile]; no max shift is needed because
+// |s| <= c bounds exp(s) by e^c.  The capped logit at the row's target column
+// is kept in fp32 (s_tgt) for the loss.
+struct EpiSoftcapCE {
+  static constexpr bool kRowReduce = true;
+  __half* s;
+  long lds;
+  float* part;
+  int n_part;
+  int tile_n;
+  const int* targets;
+  float* s_tgt;
+  float cap, inv_cap;
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+    const int y = __ldg(targets + row);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      float t;
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(v[i] * inv_cap));
+      v[i] = cap * t;
+      sum += __expf(v[i]);
+      if (col + i == y) s_tgt[row] = v[i];
+    }
+    store_row_chunk<__half, W>(s + (long)row * lds + col, v);
+    return sum;
+  }
+  __device__ __forceinline__ void row_end(int row, int col0, float sum) const {
+    part[(long)row * n_part + col0 / tile_n] = sum;
+  }
+};
+
+}  // namespace nc

@@ -1,0 +1,277 @@
+// GEMM launchers: the tcgen05 bf16 kernel (gemm_tc.cuh) and the fp32 SIMT
+// kernel used by the fp32 debug/parity mode, with the epilogue selection and
+// the deterministic split-K reduction for weight gradients.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "epilogue.cuh"
+#include "gemm_tc.cuh"
+#include "nc_internal.h"
+
+namespace nc {
+
+// ===================================================================
+// fp32 SIMT GEMM (debug mode): 64 x 64 tile, 256 threads x (4 x 4) outputs.
+// ===================================================================
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(256) gemm_f32_simt_kernel(const float* __restrict__ A, long lda,
+                                                            const float* __restrict__ B, long ldb,
+                                                            int M, int N, int K, Epi epi) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 1024; i += 256) {
+      int mm, kk;
+      if (A_MN) { mm = i & 63; kk = i >> 6; } else { kk = i & 15; mm = i >> 4; }
+      const int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < M && gk < K) v = A_MN ? A[(long)gk * lda + gm] : A[(long)gm * lda + gk];
+      As[kk][mm] = v;
+    }
+    for (int i = threadIdx.x; i < 1024; i += 256) {
+      int nn, kk;
+      if (B_MN) { nn = i & 63; kk = i >> 6; } else { kk = i & 15; nn = i >> 4; }
+      const int gn = n0 + nn, gk = k0 + kk;
+      float v = 0.f;
+      if (gn < N && gk < K) v = B_MN ? B[(long)gk * ldb + gn] : B[(long)gn * ldb + gk];
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = m0 + ty * 4 + i, col = n0 + tx * 4;
+    if (row < M && col < N) {
+      float v[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
+      epi.template apply<4>(row, col, v, 0);
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+static cudaError_t launch_f32(const GemmArgs& g, const Epi& epi, const Ctx& ctx) {
+  dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
+  gemm_f32_simt_kernel<A_MN, B_MN, Epi><<<grid, 256, 0, ctx.stream>>>(
+      static_cast<const float*>(g.A), g.lda, static_cast<const float*>(g.B), g.ldb, g.M, g.N, g.K,
+      epi);
+  return launched(1);
+}
+
+template <class Epi>
+static cudaError_t dispatch_f32(const GemmArgs& g, const Epi& epi, const Ctx& ctx) {
+  switch (g.layout) {
+    case GEMM_NT: return launch_f32<false, false>(g, epi, ctx);
+    case GEMM_NN: return launch_f32<false, true>(g, epi, ctx);
+    case GEMM_TN: return launch_f32<true, true>(g, epi, ctx);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx) {
+  switch (g.epi) {
+    case EPI_STORE: return dispatch_f32(g, EpiStore<float>{static_cast<float*>(g.C), g.ldc}, ctx);
+    case EPI_STORE_F32:
+      return dispatch_f32(g, EpiStoreF32{static_cast<float*>(g.C), g.ldc, 0, g.accumulate}, ctx);
+    case EPI_ADD_F32: return dispatch_f32(g, EpiAddF32{static_cast<float*>(g.C), g.ldc}, ctx);
+    case EPI_RELU2: return dispatch_f32(g, EpiRelu2<float>{static_cast<float*>(g.C), g.ldc}, ctx);
+    case EPI_RELU2_BWD:
+      return dispatch_f32(g,
+                          EpiRelu2Bwd<float>{static_cast<float*>(g.C),
+                                             static_cast<const float*>(g.aux), g.ldc},
+                          ctx);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ===================================================================
+// tcgen05 bf16 GEMM
+// ===================================================================
+namespace {
+
+// Work-unit count the split heuristic aims at (B300: 148 SMs).  The launch
+// itself uses the real SM count.
+constexpr int kSplitSms = 148;
+
+struct Plan {
+  tc::Sched sch;
+};
+
+Plan make_plan(int layout, int epi, int M, int N, int K, int group_m) {
+  Plan p;
+  tc::Sched& s = p.sch;
+  s.m_tiles = (M + tc::BM - 1) / tc::BM;
+  s.n_tiles = (N + tc::BN - 1) / tc::BN;
+  s.k_blocks = (K + tc::BK - 1) / tc::BK;
+  s.splits = 1;
+  s.kb_per_split = s.k_blocks;
+  const int tiles = s.m_tiles * s.n_tiles;
+  if (epi == EPI_STORE_F32 && tiles < 2 * kSplitSms && s.k_blocks >= 32) {
+    // Split the reduction so that the units fill the SMs; cost proxy =
+    // waves x k-blocks per unit, plus one k-block per split for the slab pass.
+    long best = -1;
+    for (int sp = 1; sp <= 16; ++sp) {
+      const int kbp = (s.k_blocks + sp - 1) / sp;
+      if (kbp < 8) break;
+      const int eff_splits = (s.k_blocks + kbp - 1) / kbp;
+      const int units = tiles * eff_splits;
+      const long waves = (units + kSplitSms - 1) / kSplitSms;
+      const long cost = waves * kbp + (eff_splits > 1 ? eff_splits : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        s.splits = eff_splits;
+        s.kb_per_split = kbp;
+      }
+    }
+  }
+  s.group_m = group_m > 0 ? group_m : 8;
+  s.units = tiles * s.splits;
+  (void)layout;
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major (outer x inner) matrix with row stride
+// `ld` elements; 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, long inner, long outer, long ld, int box_inner,
+               int box_outer) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ctx& ctx) {
+  CUtensorMap ta, tb;
+  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
+                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, tc::BM);
+  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
+                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::BN));
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = tc::gemm_bf16_tc_kernel<A_MN, B_MN, Epi>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = std::min(p.sch.units, ctx.num_sms);
+  kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, ctx.stream>>>(ta, tb, p.sch, g.M, g.N, epi, ctx.err,
+                                                             ctx.timeout_ns);
+  return launched(1);
+}
+
+template <class Epi>
+cudaError_t dispatch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ctx& ctx) {
+  switch (g.layout) {
+    case GEMM_NT: return launch_tc<false, false>(g, p, epi, ctx);
+    case GEMM_NN: return launch_tc<false, true>(g, p, epi, ctx);
+    case GEMM_TN: return launch_tc<true, true>(g, p, epi, ctx);
+  }
+  return cudaErrorInvalidValue;
+}
+
+__global__ void splitk_reduce_kernel(float4* __restrict__ c, const float4* __restrict__ slabs,
+                                     int splits, long n4, long slab4, int accumulate) {
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4;
+       i += (long)gridDim.x * blockDim.x) {
+    float4 s = accumulate ? c[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < splits; ++k) {
+      const float4 t = slabs[k * slab4 + i];
+      s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+    }
+    c[i] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t splitk_reduce(float* c, const float* slabs, int splits, long n, int accumulate,
+                          const Ctx& ctx) {
+  const long n4 = n / 4;
+  const int blocks = (int)std::min<long>((n4 + 255) / 256, (long)ctx.num_sms * 8);
+  splitk_reduce_kernel<<<std::max(blocks, 1), 256, 0, ctx.stream>>>(
+      reinterpret_cast<float4*>(c), reinterpret_cast<const float4*>(slabs), splits, n4, n4,
+      accumulate);
+  return launched(1);
+}
+
+size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K) {
+  Plan p = make_plan(layout, epi, M, N, K, 0);
+  return p.sch.splits > 1 ? (size_t)p.sch.splits * M * N : 0;
+}
+
+cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx) {
+  const Plan p = make_plan(g.layout, g.epi, g.M, g.N, g.K, g.group_m);
+  const bf16* aux = static_cast<const bf16*>(g.aux);
+  switch (g.epi) {
+    case EPI_STORE: return dispatch_tc(g, p, EpiStore<bf16>{static_cast<bf16*>(g.C), g.ldc}, ctx);
+    case EPI_STORE_F32: {
+      if (p.sch.splits == 1)
+        return dispatch_tc(g, p, EpiStoreF32{static_cast<float*>(g.C), g.ldc, 0, g.accumulate},
+                           ctx);
+      const size_t need = (size_t)p.sch.splits * g.M * g.N;
+      if (!g.split_buf || g.split_buf_elems < need || g.ldc != g.N) return cudaErrorInvalidValue;
+      cudaError_t e = dispatch_tc(
+          g, p, EpiStoreF32{g.split_buf, (long)g.N, (long)g.M * g.N, 0}, ctx);
+      if (e != cudaSuccess) return e;
+      return splitk_reduce(static_cast<float*>(g.C), g.split_buf, p.sch.splits, (long)g.M * g.N,
+                           g.accumulate, ctx);
+    }
+    case EPI_ADD_F32: return dispatch_tc(g, p, EpiAddF32{static_cast<float*>(g.C), g.ldc}, ctx);
+    case EPI_RELU2: return dispatch_tc(g, p, EpiRelu2<bf16>{static_cast<bf16*>(g.C), g.ldc}, ctx);
+    case EPI_RELU2_BWD:
+      return dispatch_tc(g, p, EpiRelu2Bwd<bf16>{static_cast<bf16*>(g.C), aux, g.ldc}, ctx);
+    case EPI_SOFTCAP_CE: {
+      EpiSoftcapCE e{static_cast<__half*>(g.C), g.ldc, g.part, g.n_part, tc::BN, g.targets,
+                     g.s_tgt, g.cap, 1.f / g.cap};
+      return dispatch_tc(g, p, e, ctx);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace nc

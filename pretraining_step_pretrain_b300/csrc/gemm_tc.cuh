@@ -1,0 +1,362 @@
+// Persistent bf16 GEMM on the 5th-generation tensor cores (sm_100 family,
+// built for sm_103a): TMA -> 128B-swizzled shared memory -> tcgen05.mma ->
+// fp32 accumulator in tensor memory -> tcgen05.ld -> fused epilogue.
+//
+//   C[m][n] = sum_k A(m, k) B(n, k)
+//   A(m, k) = A[m * lda + k] (K-major)  or  A[k * lda + m] (A_MN: M-major)
+//   B(n, k) = B[n * ldb + k] (K-major)  or  B[k * ldb + n] (B_MN: N-major)
+//
+// Tile 128 x 256 x 64, 4-stage shared-memory ring (48 KB a stage), two
+// 256-column TMEM accumulators so the epilogue of one tile overlaps the
+// main loop of the next.  One CTA per SM walks work units (m-tile, n-tile,
+// k-split) with a grid stride; m-tiles are visited in groups so that the
+// concurrently running CTAs share A and B tiles in L2.
+//
+// Warp roles (256 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
+// tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..7 run the epilogue
+// (warp 4 + i reads TMEM lanes 32i..32i+31, i.e. tile rows 32i..32i+31).
+// Every wait is bounded: on timeout the kernel records DEV_TIMEOUT, the
+// roles stop, in-flight copies and MMAs are drained (bounded) and TMEM is
+// released before the CTA exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "epilogue.cuh"
+#include "nc_common.cuh"
+
+namespace nc {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 256;
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+// Swizzle-128B atom: 8 rows of 128 bytes.  An MN-major operand tile is stored
+// as (BM or BN)/64 column blocks of 64 elements, each BK rows of 128 B.
+constexpr int MN_BLOCK_BYTES = BK * 128;  // 8 KB
+
+struct Sched {
+  int m_tiles, n_tiles, splits, k_blocks, kb_per_split, group_m, units;
+
+  __device__ __forceinline__ void decode(int u, int& mt, int& nt, int& split, int& kb0,
+                                         int& kb1) const {
+    const int per_split = m_tiles * n_tiles;
+    split = u / per_split;
+    const int r = u - split * per_split;
+    const int group_size = group_m * n_tiles;
+    const int group = r / group_size;
+    const int first_m = group * group_m;
+    const int gm = min(group_m, m_tiles - first_m);
+    const int in = r - group * group_size;
+    mt = first_m + in % gm;
+    nt = in / gm;
+    kb0 = split * kb_per_split;
+    kb1 = min(k_blocks, kb0 + kb_per_split);
+  }
+};
+
+// ---- PTX wrappers -------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
+// bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
+// offset >> 4, 46-48 fixed 0b001, 61-63 swizzle mode (2 = 128B).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+// K-major tile (rows of 64 K-elements = 128 B, 8-row swizzle atoms 1 KB apart):
+// LBO unused for swizzled K-major, SBO = 1 KB.  MMA step k (16 elements) starts
+// 32 B further inside the atom.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int k) {
+  return sdesc_sw128(tile + k * 32, 16, 1024);
+}
+// MN-major tile (column blocks of 64 MN-elements, BK rows of 128 B each):
+// LBO = distance between 64-wide MN blocks, SBO = distance between 8-row
+// K groups.  MMA step k covers K rows 16k..16k+15 = 2 K groups.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int k) {
+  return sdesc_sw128(tile + k * 2048, MN_BLOCK_BYTES, 1024);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+enum WaitSite : int {
+  SITE_PROD_EMPTY = 101, SITE_MMA_ACC_EMPTY = 102, SITE_MMA_FULL = 103,
+  SITE_EPI_ACC_FULL = 104, SITE_DRAIN = 105
+};
+
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const Sched sch, const int M,
+                        const int N, const Epi epi, int* err, const long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed_phase[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) armed_phase[s] = -1;
+    bool ok = true;
+    for (int u = blockIdx.x; u < sch.units && ok; u += gridDim.x) {
+      int mt, nt, split, kb0, kb1;
+      sch.decode(u, mt, nt, split, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, err, SITE_PROD_EMPTY,
+                               timeout_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        armed_phase[stage] = (int)phase;
+        uint8_t* a = sA + stage * A_BYTES;
+        uint8_t* b = sB + stage * B_BYTES;
+        const int k0 = kb * BK;
+        if (!A_MN) {
+          tma_load_2d(a, &tmA, &full[stage], k0, mt * BM);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_2d(a + j * MN_BLOCK_BYTES, &tmA, &full[stage], mt * BM + 64 * j, k0);
+        }
+        if (!B_MN) {
+          tma_load_2d(b, &tmB, &full[stage], k0, nt * BN);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(b + j * MN_BLOCK_BYTES, &tmB, &full[stage], nt * BN + 64 * j, k0);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok || *abort_flag) {
+      // Drain: let every copy this thread armed land before the CTA exits.
+      int dummy_abort = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (armed_phase[s] >= 0)
+          mbar_wait_bounded(&full[s], (uint32_t)armed_phase[s], &dummy_abort, err, SITE_DRAIN,
+                            timeout_ns / 8);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16(A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true, issued = false;
+    for (int u = blockIdx.x; u < sch.units && ok; u += gridDim.x) {
+      int mt, nt, split, kb0, kb1;
+      sch.decode(u, mt, nt, split, kb0, kb1);
+      if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, err,
+                             SITE_MMA_ACC_EMPTY, timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, err, SITE_MMA_FULL,
+                               timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = A_MN ? desc_mnmajor(a_addr, k) : desc_kmajor(a_addr, k);
+          const uint64_t bd = B_MN ? desc_mnmajor(b_addr, k) : desc_kmajor(b_addr, k);
+          umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
+        issued = true;
+        umma_commit(&empty[stage]);  // frees the smem stage once these MMAs finish
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if ((!ok || *abort_flag) && issued) {
+      // Drain: wait until every MMA issued so far has completed.
+      int dummy_abort = 0;
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, &dummy_abort, err, SITE_DRAIN, timeout_ns / 8);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < sch.units; u += gridDim.x) {
+      int mt, nt, split, kb0, kb1;
+      sch.decode(u, mt, nt, split, kb0, kb1);
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, err, SITE_EPI_ACC_FULL,
+                               timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = mt * BM + quarter * 32 + lane;
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      float row_acc = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(taddr + c * 32, v);
+        const int col = nt * BN + c * 32;
+        if (row < M && col < N) row_acc += epi.template apply<32>(row, col, v, split);
+      }
+      if (Epi::kRowReduce && row < M) epi.row_end(row, nt * BN, row_acc);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace tc
+}  // namespace nc

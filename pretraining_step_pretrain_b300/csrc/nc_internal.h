@@ -1,0 +1,97 @@
+// Internal launcher interface between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nc {
+
+struct Ctx {
+  cudaStream_t stream;
+  int* err;               // device error word (start of the workspace)
+  long long timeout_ns;   // limit of every device spin-wait
+  int num_sms;
+};
+
+// Host-side count of kernel launches issued by the library (nc_launch_count).
+void note_launch(int n);
+inline cudaError_t launched(int n) {
+  note_launch(n);
+  return cudaGetLastError();
+}
+
+enum GemmLayout { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
+enum GemmEpi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_ADD_F32 = 2, EPI_RELU2 = 3,
+               EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5 };
+
+struct GemmArgs {
+  int layout, epi;
+  int M, N, K;
+  const void* A; long lda;
+  const void* B; long ldb;
+  void* C; long ldc;
+  const void* aux;        // RELU2_BWD: saved relu(u)^2, same layout as C
+  int accumulate;         // STORE_F32: add into C
+  // SOFTCAP_CE (tensor-core path only)
+  float* part; int n_part; const int* targets; float* s_tgt; float cap;
+  // STORE_F32 split-K slabs (tensor-core path); may be null when not needed
+  float* split_buf; size_t split_buf_elems;
+  int group_m;            // m-tiles per raster group (0 = default)
+};
+
+// Tensor-core (bf16) path.
+constexpr int kTileN = 256;            // n-tile width (per-row CE partials)
+size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K);
+cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx);
+// fp32 SIMT path (debug / parity mode).
+cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx);
+
+// ---- memory-bound kernels (act = bf16 or float) ----
+// Each takes `bf16` to pick the activation type.
+cudaError_t rope_table(float2* tab, int T, int h, float base, const Ctx& ctx);
+cudaError_t embed_norm_fwd(bool bf16, const int* ids, const void* wte, float* x, float* rstd,
+                           int M, int d, int V, float eps, const Ctx& ctx);
+cudaError_t rmsnorm_fwd(bool bf16, const float* x, void* y, float* rstd, int M, int d, float eps,
+                        const Ctx& ctx);
+cudaError_t rmsnorm_bwd(bool bf16, const void* dy, const void* y, const float* rstd, float* dx,
+                        void* dx_act, int add, int M, int d, const Ctx& ctx);
+cudaError_t cast_f32_to_act(bool bf16, const float* x, void* y, long n, const Ctx& ctx);
+cudaError_t qknorm_rope_fwd(bool bf16, const void* qkv, const float2* tab, void* q, void* k,
+                            void* v, float* rstd_qk, int B, int T, int H, int h, float eps,
+                            const Ctx& ctx);
+cudaError_t qknorm_rope_bwd(bool bf16, void* dqkv, const void* q, const void* k,
+                            const float* rstd_qk, const float2* tab, int B, int T, int H, int h,
+                            const Ctx& ctx);
+cudaError_t splitk_reduce(float* c, const float* slabs, int splits, long n, int accumulate,
+                          const Ctx& ctx);
+
+// ---- attention ----
+size_t attention_scratch_bytes(int B, int T, int H);
+cudaError_t attention_fwd(bool bf16, int B, int T, int H, int h, const void* q, const void* k,
+                          const void* v, void* o, float* lse, const Ctx& ctx);
+cudaError_t attention_bwd(bool bf16, int B, int T, int H, int h, const void* q, const void* k,
+                          const void* v, const void* o, const float* lse, const void* dout,
+                          void* dq, long ldq, void* dk, long ldk, void* dv, long ldv,
+                          float* delta_scratch, const Ctx& ctx);
+
+// ---- loss ----
+cudaError_t softcap_rows_f32(float* s, const int* targets, float* lse, float* s_tgt, int M,
+                             int V, float cap, const Ctx& ctx);
+cudaError_t ce_rows_from_partials(const float* part, int n_part, float* lse, int M,
+                                  const Ctx& ctx);
+cudaError_t ce_loss(const float* lse, const float* s_tgt, const int* targets, int M, int V,
+                    float* loss, float* inv_n, const Ctx& ctx);
+cudaError_t ce_dlogits(bool bf16, void* s, const float* lse, const int* targets,
+                       const float* inv_n, int M, int V, float cap, const Ctx& ctx);
+
+// ---- embedding backward ----
+size_t embed_bwd_scratch_bytes(int M, int d);
+cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const float* rstd0,
+                           const float* dx, float* dwte, int accumulate, int M, int d, int V,
+                           void* scratch, const Ctx& ctx);
+
+// Test hook: a CTA waiting on an mbarrier nothing completes (bounded).
+cudaError_t selftest_wait(long long timeout_ns, const Ctx& ctx);
+
+}  // namespace nc

@@ -1,0 +1,321 @@
+// Memory-bound kernels of the step: parameter-free RMSNorm forward/backward,
+// the post-embedding norm, QK-norm + rotary embedding forward/backward, the
+// RoPE table and a float32 -> activation cast.  One warp per row (or per
+// (token, head)), 16-byte loads of fp32 / 8-byte loads of 16-bit data,
+// warp-shuffle reductions.  Activation type A is bf16 or float.
+//
+// RMSNorm (launch article, architecture list: RMSNorm carries no learnable
+// gain): y = x * r, r = 1/sqrt(mean(x^2) + eps).
+// Backward (from y = x r(x)): dx = r (dy - y * mean(dy * y)).
+#include "nc_common.cuh"
+#include "nc_internal.h"
+
+namespace nc {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ float rms_inv(float sumsq, int n, float eps) {
+  return rsqrtf(sumsq / (float)n + eps);
+}
+
+// ---- RoPE table: tab[t * h/2 + i] = (cos, sin)(t * base^(-2i/h)), fp64 math.
+__global__ void rope_table_kernel(float2* tab, int T, int half, int h, double base) {
+  const long n = (long)T * half;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / half), i = (int)(idx % half);
+    const double theta = pow(base, -2.0 * (double)i / (double)h);
+    double s, c;
+    sincos((double)t * theta, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+// ---- embedding gather + RMSNorm -> float32 residual.
+template <typename W>
+__global__ void embed_norm_kernel(const int* __restrict__ ids, const W* __restrict__ wte,
+                                  float* __restrict__ x, float* __restrict__ rstd, int M, int d,
+                                  int V, float eps, int* err) {
+  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const int id = ids[row];
+  float* xr = x + (long)row * d;
+  if (id < 0 || id >= V) {
+    if (lane == 0) {
+      raise_error(err, DEV_TOKEN_RANGE, 1, row);
+      rstd[row] = 0.f;
+    }
+    for (int c = lane * 4; c < d; c += 128) {
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      Vec4<float>::store(xr + c, z);
+    }
+    return;
+  }
+  const W* wr = wte + (long)id * d;
+  float ss = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float v[4];
+    Vec4<W>::load(wr + c, v);
+    ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+  }
+  const float r = rms_inv(warp_sum(ss), d, eps);
+  for (int c = lane * 4; c < d; c += 128) {
+    float v[4];
+    Vec4<W>::load(wr + c, v);
+    for (int i = 0; i < 4; ++i) v[i] *= r;
+    Vec4<float>::store(xr + c, v);
+  }
+  if (lane == 0) rstd[row] = r;
+}
+
+// ---- RMSNorm forward: float32 residual row -> activation row.
+template <typename A>
+__global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, A* __restrict__ y,
+                                   float* __restrict__ rstd, int M, int d, float eps) {
+  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const float* xr = x + (long)row * d;
+  float ss = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float v[4];
+    Vec4<float>::load(xr + c, v);
+    ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+  }
+  const float r = rms_inv(warp_sum(ss), d, eps);
+  A* yr = y + (long)row * d;
+  for (int c = lane * 4; c < d; c += 128) {
+    float v[4];
+    Vec4<float>::load(xr + c, v);
+    for (int i = 0; i < 4; ++i) v[i] *= r;
+    Vec4<A>::store(yr + c, v);
+  }
+  if (lane == 0) rstd[row] = r;
+}
+
+// ---- RMSNorm backward (+ residual): dx (+)= r (dy - y mean(dy y)); also
+// writes the activation-type copy of dx used as the next GEMM operand.
+template <typename A>
+__global__ void rmsnorm_bwd_kernel(const A* __restrict__ dy, const A* __restrict__ y,
+                                   const float* __restrict__ rstd, float* __restrict__ dx,
+                                   A* __restrict__ dx_act, int add, int M, int d) {
+  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const A* dyr = dy + (long)row * d;
+  const A* yr = y + (long)row * d;
+  float dot = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float a[4], b[4];
+    Vec4<A>::load(dyr + c, a);
+    Vec4<A>::load(yr + c, b);
+    dot += a[0] * b[0] + a[1] * b[1] + a[2] * b[2] + a[3] * b[3];
+  }
+  const float mean = warp_sum(dot) / (float)d;
+  const float r = rstd[row];
+  float* dxr = dx + (long)row * d;
+  A* dar = dx_act + (long)row * d;
+  for (int c = lane * 4; c < d; c += 128) {
+    float a[4], b[4], o[4];
+    Vec4<A>::load(dyr + c, a);
+    Vec4<A>::load(yr + c, b);
+    if (add) Vec4<float>::load(dxr + c, o);
+    for (int i = 0; i < 4; ++i) {
+      const float g = r * (a[i] - b[i] * mean);
+      o[i] = add ? o[i] + g : g;
+    }
+    Vec4<float>::store(dxr + c, o);
+    Vec4<A>::store(dar + c, o);
+  }
+}
+
+template <typename A>
+__global__ void cast_kernel(const float* __restrict__ x, A* __restrict__ y, long n4) {
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4;
+       i += (long)gridDim.x * blockDim.x) {
+    float v[4];
+    Vec4<float>::load(x + 4 * i, v);
+    Vec4<A>::store(y + 4 * i, v);
+  }
+}
+
+// ---- QK-norm + RoPE forward.  One warp per (token m, head j), j in [0, H+2):
+// j < H query heads and j == H the key head are RMS-normalised over their h
+// values and rotated; j == H+1 (value) is copied.  Lane l holds elements
+// [E l, E l + E); the rotation partner of element i < h/2 is i + h/2, held by
+// lane l ^ 16 at the same slot.
+template <typename A, int E>
+__global__ void qknorm_rope_fwd_kernel(const A* __restrict__ qkv, const float2* __restrict__ tab,
+                                       A* __restrict__ q, A* __restrict__ k, A* __restrict__ v,
+                                       float* __restrict__ rstd_qk, int M, int T, int H,
+                                       float eps) {
+  constexpr int h = 32 * E, half = h / 2;
+  const long item = blockIdx.x * (long)kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= (long)M * (H + 2)) return;
+  const int m = (int)(item / (H + 2)), j = (int)(item % (H + 2));
+  const A* src = qkv + (long)m * (H + 2) * h + (long)j * h + lane * E;
+  float x[E];
+  if (E == 4) {
+    float t[4];
+    Vec4<A>::load(src, t);
+    for (int e = 0; e < E; ++e) x[e] = t[e];
+  } else {
+    for (int e = 0; e < E; ++e) x[e] = to_f(src[e]);
+  }
+  if (j == H + 1) {
+    A* dst = v + (long)m * h + lane * E;
+    for (int e = 0; e < E; ++e) dst[e] = from_f<A>(x[e]);
+    return;
+  }
+  float ss = 0.f;
+  for (int e = 0; e < E; ++e) ss += x[e] * x[e];
+  const float r = rms_inv(warp_sum(ss), h, eps);
+  const int t = m % T;
+  const bool lo = lane < 16;
+  float out[E];
+  for (int e = 0; e < E; ++e) {
+    const float y = x[e] * r;
+    const float p = __shfl_xor_sync(0xffffffffu, y, 16);
+    const float2 cs = tab[(long)t * half + (lane & 15) * E + e];
+    out[e] = lo ? (y * cs.x - p * cs.y) : (p * cs.y + y * cs.x);
+  }
+  A* dst = (j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E;
+  if (E == 4) {
+    float t4[4] = {out[0], out[1], out[2], out[3]};
+    Vec4<A>::store(dst, t4);
+  } else {
+    for (int e = 0; e < E; ++e) dst[e] = from_f<A>(out[e]);
+  }
+  if (lane == 0) rstd_qk[(long)m * (H + 1) + j] = r;
+}
+
+// ---- QK-norm + RoPE backward, in place on the (M, (H+2)h) gradient buffer.
+// With z = R(y) the saved rotated output and g = dL/dz:
+//   dx = r * R^T (g - z * mean(g z))      (R orthogonal, so g.z = R^T g . R^T z)
+template <typename A, int E>
+__global__ void qknorm_rope_bwd_kernel(A* __restrict__ dqkv, const A* __restrict__ q,
+                                       const A* __restrict__ k, const float* __restrict__ rstd_qk,
+                                       const float2* __restrict__ tab, int M, int T, int H) {
+  constexpr int h = 32 * E, half = h / 2;
+  const long item = blockIdx.x * (long)kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= (long)M * (H + 1)) return;
+  const int m = (int)(item / (H + 1)), j = (int)(item % (H + 1));
+  A* gp = dqkv + (long)m * (H + 2) * h + (long)j * h + lane * E;
+  const A* zp = (j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E;
+  float g[E], z[E];
+  for (int e = 0; e < E; ++e) {
+    g[e] = to_f(gp[e]);
+    z[e] = to_f(zp[e]);
+  }
+  float dot = 0.f;
+  for (int e = 0; e < E; ++e) dot += g[e] * z[e];
+  const float mean = warp_sum(dot) / (float)h;
+  const float r = rstd_qk[(long)m * (H + 1) + j];
+  const int t = m % T;
+  const bool lo = lane < 16;
+  for (int e = 0; e < E; ++e) {
+    const float w = g[e] - z[e] * mean;
+    const float p = __shfl_xor_sync(0xffffffffu, w, 16);
+    const float2 cs = tab[(long)t * half + (lane & 15) * E + e];
+    const float o = lo ? (w * cs.x + p * cs.y) : (w * cs.x - p * cs.y);
+    gp[e] = from_f<A>(r * o);
+  }
+}
+
+inline int row_blocks(long rows) { return (int)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock); }
+
+}  // namespace
+
+cudaError_t rope_table(float2* tab, int T, int h, float base, const Ctx& ctx) {
+  const long n = (long)T * (h / 2);
+  const int blocks = (int)std::min<long>((n + 255) / 256, 4096);
+  rope_table_kernel<<<blocks, 256, 0, ctx.stream>>>(tab, T, h / 2, h, (double)base);
+  return launched(1);
+}
+
+cudaError_t embed_norm_fwd(bool bf16, const int* ids, const void* wte, float* x, float* rstd,
+                           int M, int d, int V, float eps, const Ctx& ctx) {
+  if (bf16)
+    embed_norm_kernel<nc::bf16><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        ids, static_cast<const nc::bf16*>(wte), x, rstd, M, d, V, eps, ctx.err);
+  else
+    embed_norm_kernel<float><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        ids, static_cast<const float*>(wte), x, rstd, M, d, V, eps, ctx.err);
+  return launched(1);
+}
+
+cudaError_t rmsnorm_fwd(bool bf16, const float* x, void* y, float* rstd, int M, int d, float eps,
+                        const Ctx& ctx) {
+  if (bf16)
+    rmsnorm_fwd_kernel<nc::bf16><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        x, static_cast<nc::bf16*>(y), rstd, M, d, eps);
+  else
+    rmsnorm_fwd_kernel<float><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        x, static_cast<float*>(y), rstd, M, d, eps);
+  return launched(1);
+}
+
+cudaError_t rmsnorm_bwd(bool bf16, const void* dy, const void* y, const float* rstd, float* dx,
+                        void* dx_act, int add, int M, int d, const Ctx& ctx) {
+  if (bf16)
+    rmsnorm_bwd_kernel<nc::bf16><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        static_cast<const nc::bf16*>(dy), static_cast<const nc::bf16*>(y), rstd, dx,
+        static_cast<nc::bf16*>(dx_act), add, M, d);
+  else
+    rmsnorm_bwd_kernel<float><<<row_blocks(M), 32 * kWarpsPerBlock, 0, ctx.stream>>>(
+        static_cast<const float*>(dy), static_cast<const float*>(y), rstd, dx,
+        static_cast<float*>(dx_act), add, M, d);
+  return launched(1);
+}
+
+cudaError_t cast_f32_to_act(bool bf16, const float* x, void* y, long n, const Ctx& ctx) {
+  const long n4 = n / 4;
+  const int blocks = (int)std::max<long>(1, std::min<long>((n4 + 255) / 256, (long)ctx.num_sms * 16));
+  if (bf16)
+    cast_kernel<nc::bf16><<<blocks, 256, 0, ctx.stream>>>(x, static_cast<nc::bf16*>(y), n4);
+  else
+    cast_kernel<float><<<blocks, 256, 0, ctx.stream>>>(x, static_cast<float*>(y), n4);
+  return launched(1);
+}
+
+cudaError_t qknorm_rope_fwd(bool bf16, const void* qkv, const float2* tab, void* q, void* k,
+                            void* v, float* rstd_qk, int B, int T, int H, int h, float eps,
+                            const Ctx& ctx) {
+  const int M = B * T;
+  const int blocks = row_blocks((long)M * (H + 2));
+#define NC_QKF(TA, EE)                                                                      \
+  qknorm_rope_fwd_kernel<TA, EE><<<blocks, 32 * kWarpsPerBlock, 0, ctx.stream>>>(          \
+      static_cast<const TA*>(qkv), tab, static_cast<TA*>(q), static_cast<TA*>(k),          \
+      static_cast<TA*>(v), rstd_qk, M, T, H, eps)
+  if (bf16) {
+    if (h == 128) NC_QKF(nc::bf16, 4); else NC_QKF(nc::bf16, 2);
+  } else {
+    if (h == 128) NC_QKF(float, 4); else NC_QKF(float, 2);
+  }
+#undef NC_QKF
+  return launched(1);
+}
+
+cudaError_t qknorm_rope_bwd(bool bf16, void* dqkv, const void* q, const void* k,
+                            const float* rstd_qk, const float2* tab, int B, int T, int H, int h,
+                            const Ctx& ctx) {
+  const int M = B * T;
+  const int blocks = row_blocks((long)M * (H + 1));
+#define NC_QKB(TA, EE)                                                                      \
+  qknorm_rope_bwd_kernel<TA, EE><<<blocks, 32 * kWarpsPerBlock, 0, ctx.stream>>>(          \
+      static_cast<TA*>(dqkv), static_cast<const TA*>(q), static_cast<const TA*>(k), rstd_qk, \
+      tab, M, T, H)
+  if (bf16) {
+    if (h == 128) NC_QKB(nc::bf16, 4); else NC_QKB(nc::bf16, 2);
+  } else {
+    if (h == 128) NC_QKB(float, 4); else NC_QKB(float, 2);
+  }
+#undef NC_QKB
+  return launched(1);
+}
+
+}  // namespace nc

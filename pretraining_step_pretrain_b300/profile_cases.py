@@ -1,0 +1,110 @@
+"""Run one kernel of the step on synthetic inputs, for profiler captures
+(ncu) and quick timing.  Every case goes through the C ABI.
+
+    python -m pretraining_step_pretrain_b300.profile_cases gemm --layout NT --epi relu2 \
+        --M 16384 --N 5120 --K 1280 --iters 3
+    python -m pretraining_step_pretrain_b300.profile_cases attn --B 4 --T 2048 --H 10 --bwd
+    python -m pretraining_step_pretrain_b300.profile_cases step --workload small_bf16
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from pretraining_step_pretrain_b300 import nc  # noqa: E402
+
+LAYOUTS = {"NT": nc.GEMM_NT, "NN": nc.GEMM_NN, "TN": nc.GEMM_TN}
+EPIS = {"store": nc.EPI_STORE, "store_f32": nc.EPI_STORE_F32, "add_f32": nc.EPI_ADD_F32,
+        "relu2": nc.EPI_RELU2, "relu2_bwd": nc.EPI_RELU2_BWD}
+
+
+def gemm(a):
+    L, E = LAYOUTS[a.layout], EPIS[a.epi]
+    M, N, K = a.M, a.N, a.K
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+    A = torch.randn(*((M, K) if L != nc.GEMM_TN else (K, M)), generator=g, device="cuda").to(bf)
+    B = (torch.randn(*((N, K) if L == nc.GEMM_NT else (K, N)), generator=g, device="cuda")
+         / K ** 0.5).to(bf)
+    lda = K if L != nc.GEMM_TN else M
+    ldb = K if L == nc.GEMM_NT else N
+    f32_out = E in (nc.EPI_STORE_F32, nc.EPI_ADD_F32)
+    C = torch.zeros(M, N, device="cuda", dtype=torch.float32 if f32_out else bf)
+    aux = torch.rand(M, N, generator=g, device="cuda").to(bf) if E == nc.EPI_RELU2_BWD else None
+    ws = None
+    for _ in range(a.iters):
+        ws = nc.gemm(nc.NC_BF16, L, E, M, N, K, A, lda, B, ldb, C, N, aux=aux, ws=ws)
+    torch.cuda.synchronize()
+    print(f"gemm {a.layout} {a.epi} M={M} N={N} K={K}: ok")
+
+
+def attn(a):
+    B, T, H, h = a.B, a.T, a.H, 128
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+    q = torch.randn(B, T, H, h, generator=g, device="cuda").to(bf)
+    k = torch.randn(B, T, h, generator=g, device="cuda").to(bf)
+    v = torch.randn(B, T, h, generator=g, device="cuda").to(bf)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, T, H, device="cuda")
+    ws = None
+    for _ in range(a.iters):
+        ws = nc.attention_fwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse, ws=ws)
+    if a.bwd:
+        do = torch.randn_like(q, dtype=torch.float32).to(bf)
+        W = (H + 2) * h
+        dqkv = torch.empty(B * T, W, dtype=bf, device="cuda")
+        for _ in range(a.iters):
+            nc.attention_bwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse, do, dqkv[:, :H * h], W,
+                             dqkv[:, H * h:H * h + h], W, dqkv[:, H * h + h:], W, ws=ws)
+    torch.cuda.synchronize()
+    print(f"attention B={B} T={T} H={H} bwd={a.bwd}: ok")
+
+
+def step(a):
+    import nc_synth
+    w = nc_synth.WORKLOADS[a.workload]
+    ids, tg = nc_synth.make_tokens(w.shape.vocab, w.batch, w.seq, seed=0, dist=w.ids)
+    st = nc.Step(w.shape, w.dtype, w.batch, w.seq,
+                 nc_synth.make_weights(w.shape, seed=1, bf16=(w.dtype == "bf16")))
+    st.ids.copy_(torch.from_numpy(ids))
+    st.targets.copy_(torch.from_numpy(tg))
+    for _ in range(a.iters):
+        st.run()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    print(f"step {a.workload}: loss {float(st.loss.item()):.5f}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    sub = ap.add_subparsers(dest="case", required=True)
+    p = sub.add_parser("gemm")
+    p.add_argument("--layout", default="NT", choices=sorted(LAYOUTS))
+    p.add_argument("--epi", default="store", choices=sorted(EPIS))
+    p.add_argument("--M", type=int, default=16384)
+    p.add_argument("--N", type=int, default=5120)
+    p.add_argument("--K", type=int, default=1280)
+    p.add_argument("--iters", type=int, default=3)
+    p = sub.add_parser("attn")
+    p.add_argument("--B", type=int, default=4)
+    p.add_argument("--T", type=int, default=2048)
+    p.add_argument("--H", type=int, default=10)
+    p.add_argument("--bwd", action="store_true")
+    p.add_argument("--iters", type=int, default=3)
+    p = sub.add_parser("step")
+    p.add_argument("--workload", default="small_bf16")
+    p.add_argument("--iters", type=int, default=2)
+    a = ap.parse_args()
+    {"gemm": gemm, "attn": attn, "step": step}[a.case](a)
+
+
+if __name__ == "__main__":
+    main()

@@ -155,10 +155,25 @@ def profile_kernels(st, steps, shape, B, T):
 
 
 # ---------------------------------------------------------------- CPU oracle
+def blas_threads() -> int:
+    """Threads the oracle's BLAS uses (threadpoolctl when present, else the
+    OpenBLAS/OMP environment, else every host core)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info()]
+        if n and max(n) > 0:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
 def oracle_tokens_per_s(shape, T, min_seconds, max_steps, weights=None):
     """Time the fp64 oracle on one row of T tokens at `shape` (host cores)."""
     import oracle
-    from threadpoolctl import threadpool_info
     if weights is None:
         weights = nc_synth.make_weights(shape, seed=1, bf16=True)
     P = {k: v.astype(np.float64) for k, v in weights.items()}
@@ -170,8 +185,7 @@ def oracle_tokens_per_s(shape, T, min_seconds, max_steps, weights=None):
         t0 = time.perf_counter()
         oracle.step(shape, P, ids, tg)
         times.append(time.perf_counter() - t0)
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    return T * len(times) / sum(times), threads, len(times)
+    return T * len(times) / sum(times), blas_threads(), len(times)
 
 
 # ---------------------------------------------------------------- arms
@@ -183,7 +197,6 @@ def run_reference(args, rank, world):
     T = args.ref_tokens
     weights = nc_synth.make_weights(shape, seed=1, bf16=True)
     import oracle
-    from threadpoolctl import threadpool_info
     P = {k: v.astype(np.float64) for k, v in weights.items()}
     ids, tg = nc_synth.make_tokens(shape.vocab, 1, T, seed=0)
     for _ in range(args.warmup):
@@ -193,7 +206,7 @@ def run_reference(args, rank, world):
         oracle.step(shape, P, ids, tg)
     dt = time.perf_counter() - t0
     value = T * args.steps / dt
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    threads = blas_threads()
     sample = f"{w.name} widths, 1 row x {T} tokens per step (fp64 numpy oracle)"
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,

@@ -174,8 +174,9 @@ const char* nc_last_error_message(void);
  *            NC_EPI_RELU2      C act type  = max(acc, 0)^2
  *            NC_EPI_RELU2_BWD  C act type  = acc * 2 sqrt(aux), aux (M,N) act
  *                              type holding relu(u)^2 (so 2 sqrt(aux) = 2 relu(u))
- * lda/ldb/ldc are row strides in elements (multiples of 8).  M, N, K >= 1,
- * N % 32 == 0, K % 8 == 0.  ws: >= nc_gemm_workspace_bytes(...). */
+ * lda/ldb/ldc are row strides in elements (multiples of 8, so every row
+ * starts 16-byte aligned).  M, N, K >= 1, N % 32 == 0; M and K may be ragged.
+ * ws: >= nc_gemm_workspace_bytes(...). */
 typedef enum { NC_GEMM_NT = 0, NC_GEMM_NN = 1, NC_GEMM_TN = 2 } nc_gemm_layout;
 typedef enum {
   NC_EPI_STORE = 0, NC_EPI_STORE_F32 = 1, NC_EPI_ADD_F32 = 2,

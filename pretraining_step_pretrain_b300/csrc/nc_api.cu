@@ -552,9 +552,8 @@ nc_status nc_gemm(int dtype, int layout, int epilogue, int M, int N, int K, cons
     return fail(NC_ERR_INVALID_ARG, "bad layout %d", layout);
   if (epilogue < NC_EPI_STORE || epilogue > NC_EPI_RELU2_BWD)
     return fail(NC_ERR_INVALID_ARG, "bad epilogue %d", epilogue);
-  if (M < 1 || N < 1 || K < 1 || N % 32 || K % 8)
-    return fail(NC_ERR_UNSUPPORTED_SHAPE, "M=%d N=%d K=%d: need >= 1, N %% 32 == 0, K %% 8 == 0",
-                M, N, K);
+  if (M < 1 || N < 1 || K < 1 || N % 32)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "M=%d N=%d K=%d: need >= 1 and N %% 32 == 0", M, N, K);
   if (lda % 8 || ldb % 8 || ldc % 8)
     return fail(NC_ERR_UNSUPPORTED_SHAPE, "leading dimensions must be multiples of 8");
   const long a_min = layout == NC_GEMM_TN ? M : K;

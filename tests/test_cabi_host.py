@@ -101,6 +101,7 @@ def test_block_calls_reject_bad_layer_index(lib):
 def test_gemm_argument_checks(lib):
     f = lib.nc_gemm
     assert f(0, 0, 0, 128, 100, 64, 4096, 64, 4096, 64, 4096, 128, None, 0, 4096, 1 << 20, None) == 2
+    assert f(0, 2, 0, 300, 128, 64, 4096, 300, 4096, 128, 4096, 128, None, 0, 4096, 1 << 20, None) == 2
     assert f(0, 7, 0, 128, 128, 64, 4096, 64, 4096, 64, 4096, 128, None, 0, 4096, 1 << 20, None) == 1
     assert f(0, 0, 9, 128, 128, 64, 4096, 64, 4096, 64, 4096, 128, None, 0, 4096, 1 << 20, None) == 1
     assert f(0, 0, 0, 128, 128, 64, 4096, 60, 4096, 64, 4096, 128, None, 0, 4096, 1 << 20, None) == 2

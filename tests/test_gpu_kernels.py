@@ -50,6 +50,10 @@ EPIS = [nc.EPI_STORE, nc.EPI_STORE_F32, nc.EPI_ADD_F32, nc.EPI_RELU2, nc.EPI_REL
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_gemm_matches_torch(dtype, layout, epi, shape):
     M, N, K = shape
+    if layout == nc.GEMM_TN:
+        # A is stored (K, M): its row stride M must be a multiple of 8; the
+        # reduction length K (tokens) stays ragged.
+        M, K = -(-M // 8) * 8, K + 13
     gen = torch.Generator(device="cuda").manual_seed(M * 7 + N * 3 + K + layout * 11 + epi)
     dt = torch.bfloat16 if dtype == "bf16" else torch.float32
     A, lda, B, ldb, ref = _operands(layout, M, N, K, dt, gen)

@@ -206,6 +206,27 @@ nc_status nc_attention_bwd(int dtype, int B, int T, int H, int h, const void* q,
                            void* dk, int ldk, void* dv, int ldv, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* Attention backward that allocates nothing and needs no workspace.  The
+ * pages have no counterpart: this is a convenience of this library for
+ * callers that cannot hand it device memory at this point -- for example an
+ * operator running inside another framework's runtime (a plugin or custom
+ * call) that owns all device memory and gives this op no scratch, or a hot
+ * loop that must not call cudaMalloc, which can synchronise the device.
+ * Arguments and results are those of nc_attention_bwd.  The per-row scratch
+ * (delta = rowsum(dO * O)) lives in one fixed device array built into the
+ * library (8 MB, held on every GPU that loads the library until the process
+ * exits), so B*T*H must be <= 2^21 query rows; larger shapes return
+ * NC_ERR_UNSUPPORTED_SHAPE without launching.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress, with the
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the array: calls that overlap on the GPU race,
+ * so order them (one stream, or events).  Each call rewrites every scratch
+ * entry it reads, so no clearing is needed between calls. */
+nc_status nc_attention_bwd_noalloc(int dtype, int B, int T, int H, int h, const void* q,
+                                   const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dout, void* dq, int ldq,
+                                   void* dk, int ldk, void* dv, int ldv, void* stream);
+
 /* ---- measurement ----------------------------------------------------------
  * Support for the throughput and roofline measurements of the step (the
  * walkthrough's "预训练" section reports model-FLOP utilisation; these calls

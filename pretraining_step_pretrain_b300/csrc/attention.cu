@@ -16,6 +16,7 @@
 // over every packed row, hence over all heads, without atomics.
 // fp32 path (debug mode, h in {64, 128}): one warp per row, plain loops.
 #include <algorithm>
+#include <mutex>
 
 #include "nc_common.cuh"
 #include "nc_internal.h"
@@ -739,6 +740,58 @@ cudaError_t attention_bwd(bool bf16, int B, int T, int H, int h, const void* q, 
       (const nc::bf16*)q, (const nc::bf16*)k, (const nc::bf16*)v, lse, (const nc::bf16*)dout,
       delta, (nc::bf16*)dk, ldk, (nc::bf16*)dv, ldv, T, H);
   return launched(2);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free attention backward.
+//
+// The backward needs one float of scratch per packed query row (delta =
+// rowsum(dO * O)).  nc_attention_bwd takes that scratch from the caller's
+// workspace; the variant below instead uses this fixed array in device
+// memory, which is part of the library image: every GPU that loads the
+// library holds these 8 MB until the process exits, and no call allocates
+// anything.  Every call shares the one array, so two calls that overlap on
+// the GPU (for example on two streams) race; callers must order them.  Each
+// call rewrites every delta entry it later reads, so nothing has to be
+// cleared between calls.
+static __device__ __align__(256) float g_noalloc_attn_delta[kNoAllocAttnMaxRows];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the array on the current device.  In host code the name
+// g_noalloc_attn_delta is only a host-side stand-in, never a device address,
+// so it is looked up here once per device (with that device current) and
+// cached.
+static cudaError_t noalloc_delta_ptr(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_attn_delta);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t attention_bwd_noalloc(bool bf16, int B, int T, int H, int h, const void* q,
+                                  const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, long ldq, void* dk, long ldk,
+                                  void* dv, long ldv, const Ctx& ctx) {
+  if ((long)B * T * H > kNoAllocAttnMaxRows) return cudaErrorInvalidValue;
+  float* delta = nullptr;
+  cudaError_t e = noalloc_delta_ptr(&delta);
+  if (e != cudaSuccess) return e;
+  return attention_bwd(bf16, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk, ldk, dv, ldv, delta,
+                       ctx);
 }
 
 }  // namespace nc

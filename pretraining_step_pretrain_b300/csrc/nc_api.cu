@@ -656,6 +656,32 @@ nc_status nc_attention_bwd(int dtype, int B, int T, int H, int h, const void* q,
   return NC_OK;
 }
 
+nc_status nc_attention_bwd_noalloc(int dtype, int B, int T, int H, int h, const void* q,
+                                   const void* k, const void* v, const void* o, const float* lse,
+                                   const void* dout, void* dq, int ldq, void* dk, int ldk,
+                                   void* dv, int ldv, void* stream) {
+  nc_status s = check_attn(dtype, B, T, H, h);
+  if (s == NC_OK) s = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv});
+  if (s != NC_OK) return s;
+  if (ldq < H * h || ldk < h || ldv < h || ldq % 8 || ldk % 8 || ldv % 8)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "bad gradient row strides");
+  if ((long)B * T * H > kNoAllocAttnMaxRows)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE,
+                "B*T*H = %ld query rows exceeds the fixed scratch of this entry point (%ld rows); "
+                "use nc_attention_bwd with a workspace",
+                (long)B * T * H, kNoAllocAttnMaxRows);
+  Ctx ctx;
+  ctx.stream = static_cast<cudaStream_t>(stream);
+  ctx.err = nullptr;  // the attention kernels record no device errors
+  ctx.timeout_ns = kWaitTimeoutNs;
+  ctx.num_sms = sm_count();
+  cudaError_t e = attention_bwd_noalloc(dtype == NC_BF16, B, T, H, h, q, k, v, o, lse, dout, dq,
+                                        ldq, dk, ldk, dv, ldv, ctx);
+  if (e != cudaSuccess)
+    return fail(NC_ERR_CUDA, "attention bwd (no-alloc): %s", cudaGetErrorString(e));
+  return NC_OK;
+}
+
 nc_status nc_selftest_wait_timeout(int timeout_us, void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < 16 || timeout_us < 1 || timeout_us > 10000000)
     return fail(NC_ERR_INVALID_ARG, "bad selftest arguments");

@@ -75,6 +75,14 @@ cudaError_t attention_bwd(bool bf16, int B, int T, int H, int h, const void* q, 
                           void* dq, long ldq, void* dk, long ldk, void* dv, long ldv,
                           float* delta_scratch, const Ctx& ctx);
 
+// Allocation-free variant: delta lives in a fixed device array of the library
+// (at most kNoAllocAttnMaxRows = B*T*H rows); see attention.cu.
+constexpr long kNoAllocAttnMaxRows = 1L << 21;
+cudaError_t attention_bwd_noalloc(bool bf16, int B, int T, int H, int h, const void* q,
+                                  const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, long ldq, void* dk, long ldk,
+                                  void* dv, long ldv, const Ctx& ctx);
+
 // ---- loss ----
 cudaError_t softcap_rows_f32(float* s, const int* targets, float* lse, float* s_tgt, int M,
                              int V, float cap, const Ctx& ctx);

@@ -25,6 +25,7 @@ EXPORTS = ("nc_workspace_bytes", "nc_embed_norm", "nc_block_fwd", "nc_lmhead_sof
            "nc_block_bwd", "nc_embed_norm_bwd", "nc_step", "nc_get_device_status",
            "nc_status_string", "nc_last_error_message", "nc_gemm_workspace_bytes", "nc_gemm",
            "nc_attention_workspace_bytes", "nc_attention_fwd", "nc_attention_bwd",
+           "nc_attention_bwd_noalloc",
            "nc_launch_count", "nc_profile_start", "nc_profile_stop", "nc_profile_record",
            "nc_selftest_wait_timeout")
 
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
             "nc_attention_workspace_bytes": (S, [I, I, I]),
             "nc_attention_fwd": (I, [I, I, I, I, I, P, P, P, P, P, P, S, P]),
             "nc_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P, I, P, I, P, I, P, S, P]),
+            "nc_attention_bwd_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, I, P, I, P, I,
+                                             P]),
             "nc_selftest_wait_timeout": (I, [I, P, S, P]),
             "nc_launch_count": (ctypes.c_longlong, []),
             "nc_profile_start": (I, [I]),
@@ -210,6 +213,14 @@ def attention_bwd(dtype, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk, ldk, dv
                               _ptr(dout), _ptr(dq), ldq, _ptr(dk), ldk, _ptr(dv), ldv, p, n,
                               _stream()))
     return ws
+
+
+def attention_bwd_noalloc(dtype, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk, ldk, dv, ldv):
+    """nc_attention_bwd without a workspace: its scratch is a fixed device
+    array inside the library (B*T*H <= 2^21; calls must not overlap)."""
+    _check(lib().nc_attention_bwd_noalloc(dtype, B, T, H, h, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                          _ptr(lse), _ptr(dout), _ptr(dq), ldq, _ptr(dk), ldk,
+                                          _ptr(dv), ldv, _stream()))
 
 
 def launch_count() -> int:

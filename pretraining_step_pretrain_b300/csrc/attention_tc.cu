@@ -1,0 +1,844 @@
+// Causal multi-query attention on the 5th-generation tensor cores (bf16,
+// head dim 128): forward, and the backward as a Q-major dQ pass plus a
+// KV-major dK/dV pass (launch article, architecture list: multi-query
+// attention -- the H query heads share one K/V head; causal for next-token
+// prediction).
+//
+// Query rows of one sequence are packed as r = t * H + head, so a tile of
+// packed rows meets a single K/V tile and every K/V byte brought on chip
+// serves all H heads; key j is visible to packed row r iff j <= r / H.
+//
+// Every kernel is warp-specialised (256 threads): warp 0 issues TMA, warp 1
+// issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..7 are the
+// softmax warps -- thread i of them owns TMEM lane i, i.e. one row of the
+// score tile, so row reductions need no shuffles.  Probabilities go from
+// registers to 128B-swizzled shared memory as the next MMA's operand.  A
+// 64-wide [row][64 dims] swizzled tile is both a K-major operand (rows = N)
+// and an MN-major one (rows = K), so no operand is ever transposed.  All
+// mbarrier waits are bounded; on timeout the CTA records DEV_TIMEOUT, stops,
+// drains in-flight copies and MMAs, and frees TMEM.
+#include <algorithm>
+
+#include "nc_common.cuh"
+#include "nc_internal.h"
+#include "tc_common.cuh"
+
+namespace nc {
+namespace {
+
+using namespace tc;
+
+constexpr int HD = 128;
+constexpr int NT = 256;  // threads per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int SITE_ATTN = 300;
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 64 bf16 values of one row into a [rows][64] 128B-swizzled atom.
+__device__ __forceinline__ void store_row_atom(uint8_t* atom, int row, const float* x) {
+  uint8_t* base = atom + row * 128;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 q;
+    q.x = pack2(x[ch * 8 + 0], x[ch * 8 + 1]);
+    q.y = pack2(x[ch * 8 + 2], x[ch * 8 + 3]);
+    q.z = pack2(x[ch * 8 + 4], x[ch * 8 + 5]);
+    q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
+    *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = q;
+  }
+}
+
+// Store 32 fp32 values as bf16 to global (64 contiguous bytes).
+__device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32], float scale) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q;
+    q.x = pack2(v[i * 8 + 0] * scale, v[i * 8 + 1] * scale);
+    q.y = pack2(v[i * 8 + 2] * scale, v[i * 8 + 3] * scale);
+    q.z = pack2(v[i * 8 + 4] * scale, v[i * 8 + 5] * scale);
+    q.w = pack2(v[i * 8 + 6] * scale, v[i * 8 + 7] * scale);
+    reinterpret_cast<uint4*>(dst)[i] = q;
+  }
+}
+
+struct CtaSync {
+  volatile int* abort_flag;
+  int* err;
+  long long timeout_ns;
+  __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) const {
+    return mbar_wait_bounded(bar, parity, abort_flag, err, SITE_ATTN, timeout_ns);
+  }
+};
+
+// ======================================================================
+// forward: 128 packed query rows per CTA, 128-key tiles
+// ======================================================================
+namespace fwd {
+constexpr int BQ = 128, BKV = 128;
+constexpr int ATOM = 16384;                 // [128 rows][64] bf16
+constexpr int Q_OFF = 0;                    // 32 KB
+constexpr int K_OFF = 32768;                // 2 x 32 KB
+constexpr int V_OFF = K_OFF + 2 * 32768;    // 2 x 32 KB
+constexpr int P_OFF = V_OFF + 2 * 32768;    // 32 KB
+constexpr int BAR_OFF = P_OFF + 32768;
+constexpr int SMEM = BAR_OFF + 256 + 1024;
+}  // namespace fwd
+
+__global__ void __launch_bounds__(NT, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ o,
+                       float* __restrict__ lse, int T, int H, int* err, long long timeout_ns) {
+  using namespace fwd;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]
+  uint64_t* s_free = bars + 11;  // [2], 128 arrivals
+  uint64_t* p_full = bars + 13;  // 128 arrivals
+  uint64_t* o_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const long TH = (long)T * H;
+  const int n_qt = (int)((TH + BQ - 1) / BQ);
+  const long r0 = (long)(n_qt - 1 - blockIdx.x) * BQ;  // heaviest tiles first
+  const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
+  const int nkv = t_last / BKV + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const CtaSync sync{abort_flag, err, timeout_ns};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    int armed[5] = {-1, -1, -1, -1, -1};  // q, k0, k1, v0, v1 parities for the drain
+    mbar_arrive_expect_tx(q_full, 2 * ATOM);
+    tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, (int)r0, b);
+    tma_load_3d(smem + Q_OFF + ATOM, &tmQ, q_full, 64, (int)r0, b);
+    armed[0] = 0;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&k_empty[st], ph ^ 1u)) break;
+      mbar_arrive_expect_tx(&k_full[st], 2 * ATOM);
+      tma_load_3d(smem + K_OFF + st * 32768, &tmK, &k_full[st], 0, j * BKV, b);
+      tma_load_3d(smem + K_OFF + st * 32768 + ATOM, &tmK, &k_full[st], 64, j * BKV, b);
+      armed[1 + st] = (int)ph;
+      if (!sync.wait(&v_empty[st], ph ^ 1u)) break;
+      mbar_arrive_expect_tx(&v_full[st], 2 * ATOM);
+      tma_load_3d(smem + V_OFF + st * 32768, &tmV, &v_full[st], 0, j * BKV, b);
+      tma_load_3d(smem + V_OFF + st * 32768 + ATOM, &tmV, &v_full[st], 64, j * BKV, b);
+      armed[3 + st] = (int)ph;
+    }
+    if (*abort_flag) {
+      int none = 0;
+      uint64_t* fb[5] = {q_full, &k_full[0], &k_full[1], &v_full[0], &v_full[1]};
+      for (int i = 0; i < 5; ++i)
+        if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
+    constexpr uint32_t idPV = idesc_bf16_mn(false, true, BQ, HD);
+    const uint32_t sQ = smem_u32(smem + Q_OFF);
+    const uint32_t sP = smem_u32(smem + P_OFF);
+    bool ok = sync.wait(q_full, 0), issued = false;
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&k_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+      tc_fence_after();
+      const uint32_t sK = smem_u32(smem + K_OFF + st * 32768);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + st * BKV, desc_k_atoms(sQ, kk, ATOM), desc_k_atoms(sK, kk, ATOM), idS,
+                  kk > 0 ? 1u : 0u);
+      umma_commit(&s_full[st]);
+      umma_commit(&k_empty[st]);
+      issued = true;
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(p_full, j & 1) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sV = smem_u32(smem + V_OFF + st * 32768);
+#pragma unroll
+      for (int kk = 0; kk < BKV / 16; ++kk)
+        umma_bf16(tmem + 256, desc_k_atoms(sP, kk, ATOM), desc_mn_blocks(sV, kk, ATOM), idPV,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(o_done);
+      umma_commit(&v_empty[st]);
+    }
+    if ((!ok || *abort_flag) && issued) {
+      int none = 0;
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax / epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const long r = r0 + row;
+    const bool valid = r < TH;
+    const int t = (int)(r / H);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = rsqrtf((float)HD) * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
+      tc_fence_after();
+      float s[BKV];
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + st * BKV + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      const int key0 = j * BKV;
+      const bool need_mask = key0 + BKV - 1 > t || key0 + BKV > T;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        float x = s[i] * sl2;
+        if (need_mask && (key0 + i > t || key0 + i >= T)) x = -INFINITY;
+        s[i] = x;
+        mx = fmaxf(mx, x);
+      }
+      // PV of the previous tile must be done before O is rescaled and before
+      // the single P buffer is overwritten.
+      if (j > 0) {
+        if (!sync.wait(o_done, (j - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (mx > m_run + 8.f) {
+        const float alpha = exp2f(m_run - mx);  // 0 on the first tile
+        if (j > 0) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float v[32];
+            tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st_32cols(tmem + lane_off + 256 + c * 32, v);
+          }
+        }
+        l_run *= alpha;
+        m_run = mx;
+      }
+      float ls = 0.f;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        const float p = exp2f(s[i] - m_run);
+        s[i] = p;
+        ls += p;
+      }
+      l_run += ls;
+      store_row_atom(smem + P_OFF, row, s);
+      store_row_atom(smem + P_OFF + ATOM, row, s + 64);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && sync.wait(o_done, (nkv - 1) & 1)) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      bf16* orow = o + ((long)b * TH + r) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
+        if (valid) store_bf16_32(orow + c * 32, v, inv);
+      }
+      if (valid) lse[(long)b * TH + r] = (m_run + log2f(l_run)) * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ======================================================================
+// backward, dQ pass: 128 packed query rows per CTA, 64-key tiles.  Also
+// writes delta = rowsum(dO * O) for the dK/dV pass.
+// ======================================================================
+namespace bdq {
+constexpr int BQ = 128, BKV = 64;
+constexpr int QATOM = 16384;   // [128 rows][64]
+constexpr int KATOM = 8192;    // [64 keys][64]
+constexpr int Q_OFF = 0;                     // 32 KB
+constexpr int DO_OFF = 32768;                // 32 KB
+constexpr int K_OFF = 65536;                 // 2 x 16 KB
+constexpr int V_OFF = K_OFF + 2 * 16384;     // 2 x 16 KB
+constexpr int DS_OFF = V_OFF + 2 * 16384;    // 16 KB ([128 rows][64 keys])
+constexpr int BAR_OFF = DS_OFF + 16384;
+constexpr int SMEM = BAR_OFF + 256 + 1024;
+}  // namespace bdq
+
+__global__ void __launch_bounds__(NT, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmDO,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ o,
+                          const bf16* __restrict__ dout, const float* __restrict__ lse,
+                          bf16* __restrict__ dq, long ldq, float* __restrict__ delta, int T, int H,
+                          int* err, long long timeout_ns) {
+  using namespace bdq;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_free = bars + 7;    // [2], 128 arrivals
+  uint64_t* ds_full = bars + 9;   // 128 arrivals
+  uint64_t* dq_done = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const long TH = (long)T * H;
+  const int n_qt = (int)((TH + BQ - 1) / BQ);
+  const long r0 = (long)(n_qt - 1 - blockIdx.x) * BQ;
+  const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
+  const int nkv = t_last / BKV + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(ds_full, 128);
+    mbar_init(dq_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const CtaSync sync{abort_flag, err, timeout_ns};
+  // TMEM columns: S[st] at 64 st, dP[st] at 128 + 64 st, dQ at 256.
+
+  if (warp == 0 && lane == 0) {
+    int armed[3] = {-1, -1, -1};
+    mbar_arrive_expect_tx(q_full, 4 * QATOM);
+    tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, (int)r0, b);
+    tma_load_3d(smem + Q_OFF + QATOM, &tmQ, q_full, 64, (int)r0, b);
+    tma_load_3d(smem + DO_OFF, &tmDO, q_full, 0, (int)r0, b);
+    tma_load_3d(smem + DO_OFF + QATOM, &tmDO, q_full, 64, (int)r0, b);
+    armed[0] = 0;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&kv_empty[st], ph ^ 1u)) break;
+      mbar_arrive_expect_tx(&kv_full[st], 4 * KATOM);
+      tma_load_3d(smem + K_OFF + st * 16384, &tmK, &kv_full[st], 0, j * BKV, b);
+      tma_load_3d(smem + K_OFF + st * 16384 + KATOM, &tmK, &kv_full[st], 64, j * BKV, b);
+      tma_load_3d(smem + V_OFF + st * 16384, &tmV, &kv_full[st], 0, j * BKV, b);
+      tma_load_3d(smem + V_OFF + st * 16384 + KATOM, &tmV, &kv_full[st], 64, j * BKV, b);
+      armed[1 + st] = (int)ph;
+    }
+    if (*abort_flag) {
+      int none = 0;
+      uint64_t* fb[3] = {q_full, &kv_full[0], &kv_full[1]};
+      for (int i = 0; i < 3; ++i)
+        if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
+    constexpr uint32_t idQ = idesc_bf16_mn(false, true, BQ, HD);
+    const uint32_t sQ = smem_u32(smem + Q_OFF), sDO = smem_u32(smem + DO_OFF);
+    const uint32_t sDS = smem_u32(smem + DS_OFF);
+    bool ok = sync.wait(q_full, 0), issued = false;
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&kv_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+      tc_fence_after();
+      const uint32_t sK = smem_u32(smem + K_OFF + st * 16384);
+      const uint32_t sV = smem_u32(smem + V_OFF + st * 16384);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + st * 64, desc_k_atoms(sQ, kk, QATOM), desc_k_atoms(sK, kk, KATOM), idS,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + 128 + st * 64, desc_k_atoms(sDO, kk, QATOM),
+                  desc_k_atoms(sV, kk, KATOM), idS, kk > 0 ? 1u : 0u);
+      umma_commit(&s_full[st]);
+      issued = true;
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+      const int st = j & 1;
+      if (!sync.wait(ds_full, j & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sK = smem_u32(smem + K_OFF + st * 16384);
+#pragma unroll
+      for (int kk = 0; kk < BKV / 16; ++kk)
+        umma_bf16(tmem + 256, desc_k_atoms(sDS, kk, QATOM), desc_mn_blocks(sK, kk, KATOM), idQ,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(dq_done);
+      umma_commit(&kv_empty[st]);
+    }
+    if ((!ok || *abort_flag) && issued) {
+      int none = 0;
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const long r = r0 + row;
+    const bool valid = r < TH;
+    const int t = (int)(r / H);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = rsqrtf((float)HD) * kLog2e;
+    const long grow = (long)b * TH + r;
+    float dl = 0.f, lse2 = 0.f;
+    if (valid) {
+      const bf16* orow = o + grow * HD;
+      const bf16* drow = dout + grow * HD;
+#pragma unroll 4
+      for (int i = 0; i < HD; i += 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(orow + i);
+        const uint4 d = *reinterpret_cast<const uint4*>(drow + i);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 fa = __bfloat1622float2(a2[k]), fd = __bfloat1622float2(d2[k]);
+          dl += fa.x * fd.x + fa.y * fd.y;
+        }
+      }
+      delta[grow] = dl;
+      lse2 = lse[grow] * kLog2e;
+    }
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
+      tc_fence_after();
+      float s[BKV], dp[BKV];
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + st * 64 + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+        tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dp[c * 32 + i] = v[i];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      const int key0 = j * BKV;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        float p = exp2f(s[i] * sl2 - lse2);
+        if (!valid || key0 + i > t || key0 + i >= T) p = 0.f;
+        s[i] = p * (dp[i] - dl);
+      }
+      if (j > 0) {  // the dQ MMA of the previous tile has read the dS buffer
+        if (!sync.wait(dq_done, (j - 1) & 1)) { ok = false; break; }
+      }
+      store_row_atom(smem + DS_OFF, row, s);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && sync.wait(dq_done, (nkv - 1) & 1)) {
+      tc_fence_after();
+      const float scale = rsqrtf((float)HD);
+      bf16* qrow = dq + ((long)b * T + t) * ldq + (long)(r % H) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
+        if (valid) store_bf16_32(qrow + c * 32, v, scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ======================================================================
+// backward, dK/dV pass: 128 keys per CTA, 64-row query tiles over every
+// packed row that can see them (all heads: the MQA head sum).
+// ======================================================================
+namespace bkv {
+constexpr int BKV = 128, BQ = 64;
+constexpr int KATOM = 16384;   // [128 keys][64]
+constexpr int QATOM = 8192;    // [64 rows][64]
+constexpr int K_OFF = 0;                      // 32 KB
+constexpr int V_OFF = 32768;                  // 32 KB
+constexpr int Q_OFF = 65536;                  // 2 x 16 KB
+constexpr int DO_OFF = Q_OFF + 2 * 16384;     // 2 x 16 KB
+constexpr int PT_OFF = DO_OFF + 2 * 16384;    // 16 KB ([128 keys][64 rows])
+constexpr int DST_OFF = PT_OFF + 16384;       // 16 KB
+constexpr int INFO_OFF = DST_OFF + 16384;     // [2][64] x (lse2, delta, tok)
+constexpr int BAR_OFF = INFO_OFF + 2 * 64 * 12 + 128;
+constexpr int SMEM = BAR_OFF + 256 + 1024;
+}  // namespace bkv
+
+__global__ void __launch_bounds__(NT, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmDO,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const float* __restrict__ lse,
+                            const float* __restrict__ delta, bf16* __restrict__ dk, long ldk,
+                            bf16* __restrict__ dv, long ldv, int T, int H, int* err,
+                            long long timeout_ns) {
+  using namespace bkv;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;   // [2]
+  uint64_t* q_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;   // [2]
+  uint64_t* s_free = bars + 7;   // [2], 128 arrivals
+  uint64_t* p_full = bars + 9;   // 128 arrivals
+  uint64_t* pd_done = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint64_t* info_full = bars + 12;  // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 14;  // [2], 128 arrivals
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][64]
+  float* info_dl = info_lse + 2 * 64;                                 // [2][64]
+  int* info_tok = reinterpret_cast<int*>(info_dl + 2 * 64);           // [2][64]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int j0 = blockIdx.x * BKV;
+  const long TH = (long)T * H;
+  const long rt0 = ((long)j0 * H) / BQ;
+  const int n_rt = (int)((TH + BQ - 1) / BQ - rt0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pd_done, 1);
+    mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&info_full[i], 32);
+      mbar_init(&info_free[i], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const CtaSync sync{abort_flag, err, timeout_ns};
+  // TMEM columns: St[st] at 64 st, dPt[st] at 128 + 64 st, dV at 256, dK at 384.
+
+  if (warp == 3) {
+    // ------------------------------------------------ per-row data of each query tile
+    for (int i = 0; i < n_rt; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!sync.wait(&info_free[st], ph ^ 1u)) break;
+      for (int c = lane; c < BQ; c += 32) {
+        const long rr = (rt0 + i) * BQ + c;
+        const bool v = rr < TH;
+        info_lse[st * 64 + c] = v ? lse[(long)b * TH + rr] * kLog2e : 0.f;
+        info_dl[st * 64 + c] = v ? delta[(long)b * TH + rr] : 0.f;
+        info_tok[st * 64 + c] = v ? (int)(rr / H) : -1;
+      }
+      mbar_arrive(&info_full[st]);
+    }
+  }
+
+  if (warp == 0 && lane == 0) {
+    int armed[3] = {-1, -1, -1};
+    mbar_arrive_expect_tx(kv_full, 4 * KATOM);
+    tma_load_3d(smem + K_OFF, &tmK, kv_full, 0, j0, b);
+    tma_load_3d(smem + K_OFF + KATOM, &tmK, kv_full, 64, j0, b);
+    tma_load_3d(smem + V_OFF, &tmV, kv_full, 0, j0, b);
+    tma_load_3d(smem + V_OFF + KATOM, &tmV, kv_full, 64, j0, b);
+    armed[0] = 0;
+    for (int i = 0; i < n_rt; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      const int rr = (int)((rt0 + i) * BQ);
+      if (!sync.wait(&q_empty[st], ph ^ 1u)) break;
+      mbar_arrive_expect_tx(&q_full[st], 4 * QATOM);
+      tma_load_3d(smem + Q_OFF + st * 16384, &tmQ, &q_full[st], 0, rr, b);
+      tma_load_3d(smem + Q_OFF + st * 16384 + QATOM, &tmQ, &q_full[st], 64, rr, b);
+      tma_load_3d(smem + DO_OFF + st * 16384, &tmDO, &q_full[st], 0, rr, b);
+      tma_load_3d(smem + DO_OFF + st * 16384 + QATOM, &tmDO, &q_full[st], 64, rr, b);
+      armed[1 + st] = (int)ph;
+    }
+    if (*abort_flag) {
+      int none = 0;
+      uint64_t* fb[3] = {kv_full, &q_full[0], &q_full[1]};
+      for (int i = 0; i < 3; ++i)
+        if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
+    constexpr uint32_t idG = idesc_bf16_mn(false, true, BKV, HD);
+    const uint32_t sK = smem_u32(smem + K_OFF), sV = smem_u32(smem + V_OFF);
+    const uint32_t sPt = smem_u32(smem + PT_OFF), sdSt = smem_u32(smem + DST_OFF);
+    bool ok = sync.wait(kv_full, 0), issued = false;
+    auto issue_s = [&](int i) -> bool {
+      const int st = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!sync.wait(&q_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(smem + Q_OFF + st * 16384);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + st * 16384);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + st * 64, desc_k_atoms(sK, kk, KATOM), desc_k_atoms(sQ, kk, QATOM), idS,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + 128 + st * 64, desc_k_atoms(sV, kk, KATOM),
+                  desc_k_atoms(sDO, kk, QATOM), idS, kk > 0 ? 1u : 0u);
+      umma_commit(&s_full[st]);
+      issued = true;
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int i = 0; ok && i < n_rt; ++i) {
+      if (i + 1 < n_rt && !issue_s(i + 1)) { ok = false; break; }
+      const int st = i & 1;
+      if (!sync.wait(p_full, i & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(smem + Q_OFF + st * 16384);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + st * 16384);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk)
+        umma_bf16(tmem + 256, desc_k_atoms(sPt, kk, KATOM), desc_mn_blocks(sDO, kk, QATOM), idG,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk)
+        umma_bf16(tmem + 384, desc_k_atoms(sdSt, kk, KATOM), desc_mn_blocks(sQ, kk, QATOM), idG,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(pd_done);
+      umma_commit(&q_empty[st]);
+    }
+    if ((!ok || *abort_flag) && issued) {
+      int none = 0;
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int krow = quarter * 32 + lane;  // key inside the tile
+    const int key = j0 + krow;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = rsqrtf((float)HD) * kLog2e;
+    bool ok = true;
+    for (int i = 0; i < n_rt; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!sync.wait(&s_full[st], ph) || !sync.wait(&info_full[st], ph)) { ok = false; break; }
+      tc_fence_after();
+      float s[BQ], dp[BQ];
+#pragma unroll
+      for (int c = 0; c < BQ / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + st * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[c * 32 + k] = v[k];
+        tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dp[c * 32 + k] = v[k];
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+#pragma unroll
+      for (int c = 0; c < BQ; ++c) {
+        float p = exp2f(s[c] * sl2 - info_lse[st * 64 + c]);
+        if (key > info_tok[st * 64 + c] || key >= T) p = 0.f;
+        s[c] = p;
+        dp[c] = p * (dp[c] - info_dl[st * 64 + c]);
+      }
+      mbar_arrive(&info_free[st]);
+      if (i > 0) {  // dV/dK MMAs of the previous tile have read P^T, dS^T
+        if (!sync.wait(pd_done, (i - 1) & 1)) { ok = false; break; }
+      }
+      store_row_atom(smem + PT_OFF, krow, s);
+      store_row_atom(smem + DST_OFF, krow, dp);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && n_rt > 0 && sync.wait(pd_done, (n_rt - 1) & 1)) {
+      tc_fence_after();
+      const float scale = rsqrtf((float)HD);
+      const bool valid = key < T;
+      const long tok = (long)b * T + key;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
+        if (valid) store_bf16_32(dv + tok * ldv + c * 32, v, 1.f);
+        tmem_ld_32cols(tmem + lane_off + 384 + c * 32, v);
+        if (valid) store_bf16_32(dk + tok * ldk + c * 32, v, scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// 3-D map over a (B, rows, 128) bf16 tensor: box {64, box_rows, 1}; rows past
+// `rows` read as zero, so a tile never sees the next sequence.
+bool map3(CUtensorMap* m, const void* base, long rows, int B, int box_rows) {
+  const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)rows, (uint64_t)B};
+  const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)rows * HD * 2};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+  return make_tmap_bf16(m, base, 3, dims, strides, box);
+}
+
+template <class K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+cudaError_t attention_fwd_tc(int B, int T, int H, const void* q, const void* k, const void* v,
+                             void* o, float* lse, const Ctx& ctx) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(attn_fwd_tc_kernel, fwd::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const long TH = (long)T * H;
+  CUtensorMap mq, mk, mv;
+  if (!map3(&mq, q, TH, B, fwd::BQ) || !map3(&mk, k, T, B, fwd::BKV) ||
+      !map3(&mv, v, T, B, fwd::BKV))
+    return cudaErrorInvalidValue;
+  dim3 grid((unsigned)((TH + fwd::BQ - 1) / fwd::BQ), B);
+  attn_fwd_tc_kernel<<<grid, NT, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, T, H,
+                                                          ctx.err, ctx.timeout_ns);
+  return launched(1);
+}
+
+cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, const void* v,
+                             const void* o, const float* lse, const void* dout, void* dq,
+                             long ldq, void* dk, long ldk, void* dv, long ldv, float* delta,
+                             const Ctx& ctx) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(attn_bwd_dq_tc_kernel, bdq::SMEM);
+    if (e == cudaSuccess) e = set_smem(attn_bwd_dkdv_tc_kernel, bkv::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const long TH = (long)T * H;
+  CUtensorMap mq, mdo, mk, mv;
+  if (!map3(&mq, q, TH, B, bdq::BQ) || !map3(&mdo, dout, TH, B, bdq::BQ) ||
+      !map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV))
+    return cudaErrorInvalidValue;
+  dim3 gq((unsigned)((TH + bdq::BQ - 1) / bdq::BQ), B);
+  attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
+      mq, mdo, mk, mv, (const nc::bf16*)o, (const nc::bf16*)dout, lse, (nc::bf16*)dq, ldq, delta,
+      T, H, ctx.err, ctx.timeout_ns);
+  note_launch(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ) ||
+      !map3(&mk, k, T, B, bkv::BKV) || !map3(&mv, v, T, B, bkv::BKV))
+    return cudaErrorInvalidValue;
+  dim3 gk((unsigned)((T + bkv::BKV - 1) / bkv::BKV), B);
+  attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(mq, mdo, mk, mv, lse, delta,
+                                                             (nc::bf16*)dk, ldk, (nc::bf16*)dv,
+                                                             ldv, T, H, ctx.err, ctx.timeout_ns);
+  return launched(1);
+}
+
+}  // namespace nc

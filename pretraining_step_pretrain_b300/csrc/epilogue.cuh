@@ -110,9 +110,33 @@ struct EpiRelu2 {
 template <typename TOut>
 struct EpiRelu2Bwd {
   static constexpr bool kRowReduce = false;
+  // The tensor-core epilogue loads this tile row's `a` slice before it waits
+  // for the accumulator, so the global-load latency overlaps the main loop.
+  static constexpr bool kPrefetch = true;
+  struct Pre {
+    uint4 q[32 * sizeof(TOut) / 16];  // 32 elements of a
+  };
   TOut* du;
   const TOut* a;
   long ld;
+  __device__ __forceinline__ static float two_sqrt(float x) {
+    float r;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return 2.f * r;
+  }
+  __device__ __forceinline__ void prefetch(int row, int col, Pre& p) const {
+    const uint4* src = reinterpret_cast<const uint4*>(a + (long)row * ld + col);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(Pre) / 16); ++i) p.q[i] = __ldg(src + i);
+  }
+  __device__ __forceinline__ float apply_pre(int row, int col, float (&v)[32], int,
+                                             const Pre& p) const {
+    const TOut* av = reinterpret_cast<const TOut*>(p.q);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= two_sqrt(to_f(av[i]));
+    store_row_chunk<TOut, 32>(du + (long)row * ld + col, v);
+    return 0.f;
+  }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
     float av[W];

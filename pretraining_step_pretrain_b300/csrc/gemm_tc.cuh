@@ -22,8 +22,11 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "epilogue.cuh"
 #include "nc_common.cuh"
+#include "tc_common.cuh"
 
 namespace nc {
 namespace tc {
@@ -62,83 +65,6 @@ struct Sched {
   }
 };
 
-// ---- PTX wrappers -------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
-// bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
-// offset >> 4, 46-48 fixed 0b001, 61-63 swizzle mode (2 = 128B).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
 // K-major tile (rows of 64 K-elements = 128 B, 8-row swizzle atoms 1 KB apart):
 // LBO unused for swizzled K-major, SBO = 1 KB.  MMA step k (16 elements) starts
 // 32 B further inside the atom.
@@ -157,6 +83,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+
+// Epilogues that declare kPrefetch load their per-row operand for the whole
+// tile before waiting for the accumulator.
+template <class E, class = void>
+struct HasPrefetch {
+  static constexpr bool value = false;
+};
+template <class E>
+struct HasPrefetch<E, std::void_t<decltype(E::kPrefetch)>> {
+  static constexpr bool value = E::kPrefetch;
+};
+struct NoPre {};
+template <class E, bool kPre>
+struct PreOf {
+  using type = NoPre;
+};
+template <class E>
+struct PreOf<E, true> {
+  using type = typename E::Pre;
+};
 
 enum WaitSite : int {
   SITE_PROD_EMPTY = 101, SITE_MMA_ACC_EMPTY = 102, SITE_MMA_FULL = 103,
@@ -321,6 +267,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int u = blockIdx.x; u < sch.units; u += gridDim.x) {
       int mt, nt, split, kb0, kb1;
       sch.decode(u, mt, nt, split, kb0, kb1);
+      const int row = mt * BM + quarter * 32 + lane;
+      constexpr bool kPre = HasPrefetch<Epi>::value;
+      using Pre = typename std::conditional<kPre, typename PreOf<Epi, kPre>::type, NoPre>::type;
+      Pre pre[kPre ? BN / 32 : 1];
+      if constexpr (kPre) {
+        if (row < M) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            if (nt * BN + c * 32 < N) epi.prefetch(row, nt * BN + c * 32, pre[c]);
+        }
+      }
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, err, SITE_EPI_ACC_FULL,
@@ -328,16 +285,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int row = mt * BM + quarter * 32 + lane;
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       float row_acc = 0.f;
+      if constexpr (kPre) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld_32cols(taddr + c * 32, v);
+          const int col = nt * BN + c * 32;
+          if (row < M && col < N) row_acc += epi.apply_pre(row, col, v, split, pre[c]);
+        }
+      } else {
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld_32cols(taddr + c * 32, v);
-        const int col = nt * BN + c * 32;
-        if (row < M && col < N) row_acc += epi.template apply<32>(row, col, v, split);
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld_32cols(taddr + c * 32, v);
+          const int col = nt * BN + c * 32;
+          if (row < M && col < N) row_acc += epi.template apply<32>(row, col, v, split);
+        }
       }
       if (Epi::kRowReduce && row < M) epi.row_end(row, nt * BN, row_acc);
       tc_fence_before();

@@ -17,7 +17,10 @@ typedef __nv_bfloat16 bf16;
 //   word[2] detail (offending token index, ...)
 enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_TOKEN_RANGE = 6 };
 
+// A null word (a caller with no workspace) records nothing; the kernel still
+// stops the work that failed.
 __device__ __forceinline__ void raise_error(int* err, int code, int site, int detail) {
+  if (err == nullptr) return;
   if (atomicCAS(err, 0, code) == 0) {
     err[1] = site;
     err[2] = detail;

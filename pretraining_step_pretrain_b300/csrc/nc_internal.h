@@ -1,6 +1,7 @@
 // Internal launcher interface between the C-ABI host code and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -40,6 +41,11 @@ struct GemmArgs {
   int group_m;            // m-tiles per raster group (0 = default)
 };
 
+// bf16 tensor map with 128-byte swizzle and zero fill out of range.  dims[0]
+// is the contiguous extent; strides_bytes has rank - 1 entries.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
 // Tensor-core (bf16) path.
 constexpr int kTileN = 256;            // n-tile width (per-row CE partials)
 size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K);
@@ -75,6 +81,13 @@ cudaError_t attention_bwd(bool bf16, int B, int T, int H, int h, const void* q, 
                           void* dq, long ldq, void* dk, long ldk, void* dv, long ldv,
                           float* delta_scratch, const Ctx& ctx);
 
+// tcgen05 kernels behind the bf16 path (attention_tc.cu), head dim 128.
+cudaError_t attention_fwd_tc(int B, int T, int H, const void* q, const void* k, const void* v,
+                             void* o, float* lse, const Ctx& ctx);
+cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, const void* v,
+                             const void* o, const float* lse, const void* dout, void* dq,
+                             long ldq, void* dk, long ldk, void* dv, long ldv, float* delta,
+                             const Ctx& ctx);
 // Allocation-free variant: delta lives in a fixed device array of the library
 // (at most kNoAllocAttnMaxRows = B*T*H rows); see attention.cu.
 constexpr long kNoAllocAttnMaxRows = 1L << 21;

@@ -134,39 +134,132 @@ __global__ void radix_scatter_kernel(const uint32_t* __restrict__ keys_in,
   }
 }
 
-// One CTA per vocabulary row: sum its (sorted) tokens in token order.
-__global__ void segment_sum_kernel(const uint32_t* __restrict__ keys,
-                                   const uint32_t* __restrict__ vals,
-                                   const float* __restrict__ dx0, float* __restrict__ dwte, int M,
-                                   int d, int accumulate) {
-  __shared__ int range[2];
-  const uint32_t v = blockIdx.x;
-  if (threadIdx.x < 2) {
-    const uint32_t target = v + threadIdx.x;  // lower_bound(v), lower_bound(v + 1)
+// Segmented sum over the sorted token list, cut into fixed slices of kSlice
+// tokens (one CTA each).  Inside a slice every run of equal ids is summed in
+// token order.  A run that is a whole segment (its neighbours on both sides
+// carry other ids) is written to dwte directly; a run cut by a slice edge is
+// a partial: the first run of slice s goes to part_first[s], the last to
+// part_last[s] (a slice that is one single cut run uses part_first).
+constexpr int kSlice = 64;
+constexpr int kSegThreads = 128;
+
+__global__ void __launch_bounds__(kSegThreads)
+    segment_slice_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals,
+                         const float* __restrict__ dx0, float* __restrict__ dwte,
+                         float* __restrict__ part_first, float* __restrict__ part_last, int M,
+                         int d, int accumulate) {
+  __shared__ uint32_t k_s[kSlice], v_s[kSlice];
+  const int s = blockIdx.x;
+  const int i0 = s * kSlice, n = min(kSlice, M - i0);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    k_s[i] = keys[i0 + i];
+    v_s[i] = vals[i0 + i];
+  }
+  const uint32_t prev = i0 > 0 ? keys[i0 - 1] : 0xFFFFFFFFu;
+  const uint32_t next = i0 + n < M ? keys[i0 + n] : 0xFFFFFFFFu;
+  __syncthreads();
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int run0 = 0;
+    for (int g = 0; g < n; g += 8) {
+      float t[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (g + j < n) Vec4<float>::load(dx0 + (long)v_s[g + j] * d + c, t[j]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = g + j;
+        if (i >= n) break;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] += t[j][k];
+        const uint32_t v = k_s[i];
+        const uint32_t after = i + 1 < n ? k_s[i + 1] : next;
+        if (after == v) continue;  // the run goes on
+        // The run ends at i.  It is a whole segment unless it began before
+        // this slice; such a run is the slice's first run (a partial).
+        float* out;
+        if (run0 > 0 || prev != v) {
+          out = dwte + (long)v * d + c;
+          if (accumulate) {
+            float o[4];
+            Vec4<float>::load(out, o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] += o[k];
+          }
+        } else {
+          out = part_first + (long)s * d + c;
+        }
+        Vec4<float>::store(out, acc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = 0.f;
+        run0 = i + 1;
+      }
+    }
+    if (run0 < n) {
+      // The last run continues into the next slice.
+      float* out = (run0 == 0 ? part_first : part_last) + (long)s * d;
+      Vec4<float>::store(out + c, acc);
+    }
+  }
+}
+
+// One CTA per slice: if a segment cut by slice edges starts in this slice,
+// sum its partials slice by slice (fixed order) and write its dwte row.
+__global__ void __launch_bounds__(kSegThreads)
+    segment_join_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ part_first,
+                        const float* __restrict__ part_last, float* __restrict__ dwte, int M,
+                        int d, int accumulate) {
+  const int s = blockIdx.x;
+  const int i0 = s * kSlice, n = min(kSlice, M - i0);
+  const uint32_t v = keys[i0 + n - 1];
+  if (i0 + n >= M || keys[i0 + n] != v) return;  // the last run ends in this slice
+  const bool whole_slice = keys[i0] == v;
+  if (whole_slice && i0 > 0 && keys[i0 - 1] == v) return;  // began in an earlier slice
+  const int nslices = (M + kSlice - 1) / kSlice;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    float acc[4];
+    Vec4<float>::load((whole_slice ? part_first : part_last) + (long)s * d + c, acc);
+    for (int s2 = s + 1; s2 < nslices; ++s2) {
+      float t[4];
+      Vec4<float>::load(part_first + (long)s2 * d + c, t);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += t[k];
+      const int e2 = min(M, (s2 + 1) * kSlice);
+      if (keys[e2 - 1] != v || e2 >= M || keys[e2] != v) break;  // the segment ends here
+    }
+    float* out = dwte + (long)v * d + c;
+    if (accumulate) {
+      float o[4];
+      Vec4<float>::load(out, o);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += o[k];
+    }
+    Vec4<float>::store(out, acc);
+  }
+}
+
+// Rows of dwte whose id occurs in no token: zero (or left as they are when
+// accumulating).  One warp per vocabulary row; lane 0 binary-searches the
+// sorted ids.
+__global__ void segment_zero_kernel(const uint32_t* __restrict__ keys, float* __restrict__ dwte,
+                                    int M, int d, int V) {
+  const int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (v >= V) return;
+  int present = 0;
+  if (lane == 0) {
     int lo = 0, hi = M;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (keys[mid] < target) lo = mid + 1; else hi = mid;
+      if (keys[mid] < (uint32_t)v) lo = mid + 1; else hi = mid;
     }
-    range[threadIdx.x] = lo;
+    present = lo < M && keys[lo] == (uint32_t)v;
   }
-  __syncthreads();
-  const int b = range[0], e = range[1];
+  present = __shfl_sync(0xffffffffu, present, 0);
+  if (present) return;
   float* out = dwte + (long)v * d;
-  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = b; i < e; ++i) {
-      float t[4];
-      Vec4<float>::load(dx0 + (long)vals[i] * d + c, t);
-      for (int k = 0; k < 4; ++k) acc[k] += t[k];
-    }
-    if (accumulate) {
-      float o[4];
-      Vec4<float>::load(out + c, o);
-      for (int k = 0; k < 4; ++k) acc[k] += o[k];
-    }
-    Vec4<float>::store(out + c, acc);
-  }
+  const float z[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = lane * 4; c < d; c += 128) Vec4<float>::store(out + c, z);
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -175,8 +268,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t embed_bwd_scratch_bytes(int M, int d) {
   const int ntiles = (M + kSortTile - 1) / kSortTile;
+  const size_t nslices = (M + kSlice - 1) / kSlice;
   return align256((size_t)M * d * 4) + 4 * align256((size_t)M * 4) +
-         align256((size_t)256 * ntiles * 4);
+         align256((size_t)256 * ntiles * 4) + 2 * align256(nslices * d * 4);
 }
 
 cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const float* rstd0,
@@ -190,6 +284,11 @@ cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const flo
   uint32_t* k1 = reinterpret_cast<uint32_t*>(p); p += align256((size_t)M * 4);
   uint32_t* v1 = reinterpret_cast<uint32_t*>(p); p += align256((size_t)M * 4);
   uint32_t* hist = reinterpret_cast<uint32_t*>(p);
+  const int ntiles_ = (M + kSortTile - 1) / kSortTile;
+  p += align256((size_t)256 * ntiles_ * 4);
+  const int nslices = (M + kSlice - 1) / kSlice;
+  float* part_first = reinterpret_cast<float*>(p); p += align256((size_t)nslices * d * 4);
+  float* part_last = reinterpret_cast<float*>(p);
   const int ntiles = (M + kSortTile - 1) / kSortTile;
 
   const int rblocks = (M + 7) / 8;
@@ -215,8 +314,15 @@ cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const flo
     std::swap(v0, v1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  segment_sum_kernel<<<V, 128, 0, ctx.stream>>>(k0, v0, dx0, dwte, M, d, accumulate);
-  return launched(1);
+  if (!accumulate) {
+    segment_zero_kernel<<<(V + 7) / 8, 256, 0, ctx.stream>>>(k0, dwte, M, d, V);
+    note_launch(1);
+  }
+  segment_slice_kernel<<<nslices, kSegThreads, 0, ctx.stream>>>(k0, v0, dx0, dwte, part_first,
+                                                                part_last, M, d, accumulate);
+  segment_join_kernel<<<nslices, kSegThreads, 0, ctx.stream>>>(k0, part_first, part_last, dwte, M,
+                                                               d, accumulate);
+  return launched(2);
 }
 
 }  // namespace nc

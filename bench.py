@@ -136,14 +136,8 @@ def algorithmic_cost(name, shape, B, T):
     return None, 0
 
 
-def profile_kernels(st, steps, shape, B, T):
-    from pretraining_step_pretrain_b300 import nc
-    import torch
-    nc.profile_start(200 * (shape.depth + 2) * steps)
-    for _ in range(steps):
-        st.run()
-    torch.cuda.synchronize()
-    recs = nc.profile_stop()
+def aggregate_profile(recs):
+    """[(launch group, ms)] -> rows sorted by total time, and the total."""
     agg = {}
     for name, ms in recs:
         a = agg.setdefault(name, [0.0, 0])
@@ -152,6 +146,34 @@ def profile_kernels(st, steps, shape, B, T):
     total = sum(v[0] for v in agg.values())
     rows = sorted(agg.items(), key=lambda kv: -kv[1][0])
     return rows, total
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+
+
+def measured_traffic(group):
+    """DRAM bytes per launch of a launch group from an ncu capture listed in
+    profiles/roofline_traffic.txt, or None when there is none or a listed
+    kernel source changed since the capture (its sha256 prefix differs)."""
+    import hashlib
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) < 4 or parts[0].startswith("#") or parts[0] != group:
+                continue
+            h = hashlib.sha256()
+            for src in parts[3:]:
+                path = os.path.join(ROOT, "pretraining_step_pretrain_b300", "csrc", src)
+                if not os.path.exists(path):
+                    return None
+                with open(path, "rb") as g:
+                    h.update(g.read())
+            if h.hexdigest()[:16] != parts[2]:
+                return None
+            return float(parts[1])
+    return None
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -261,6 +283,9 @@ def run_ours(args, rank, world, local_rank):
     if local_rank < len(visible) and visible[local_rank].isdigit():
         gpu_idx = int(visible[local_rank])
     clocks = ClockSampler(gpu_idx)
+    # Per-launch-group CUDA events (recorded by the library on the launching
+    # stream, events created beforehand) over the timed steps themselves.
+    nc.profile_start(60 * (shape.depth + 2) * args.steps)
     barrier()
     clocks.start()
     n0 = nc.launch_count()
@@ -270,6 +295,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     launches = nc.launch_count() - n0
+    recs = nc.profile_stop()
     clk = clocks.stop()
     barrier()
     ms = e0.elapsed_time(e1)
@@ -299,8 +325,8 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
            "d2h_bytes_per_step": 4}
 
-    # per-kernel attribution (separate, profiled steps)
-    rows, prof_total = profile_kernels(st, args.profile_steps, shape, B, T)
+    # per-launch-group attribution over the timed steps
+    rows, prof_total = aggregate_profile(recs)
     peaks, peak_src = load_peaks()
     top = None
     for name, (tot, cnt) in rows:
@@ -316,20 +342,22 @@ def run_ours(args, rank, world, local_rank):
             achieved = amount / per_launch_s / 1e12
             peak = peaks["bf16_tflops_sustained"]
             roofline = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
-                        "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                        "unit": "TFLOP/s", "frac": achieved / peak,
+                        "traffic": measured_traffic(name),
                         "peak_source": f"{peak_src} bf16 sustained", "share": tot / prof_total,
                         "algorithmic_per_launch": amount}
         else:
             achieved = amount / per_launch_s / 1e9
             peak = peaks["hbm_gbs"]
             roofline = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": peak,
-                        "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                        "unit": "GB/s", "frac": achieved / peak,
+                        "traffic": measured_traffic(name),
                         "peak_source": f"{peak_src} copy bandwidth", "share": tot / prof_total,
                         "algorithmic_per_launch": amount}
     kernels = []
     for name, (tot, cnt) in rows[:12]:
         kind, amount = algorithmic_cost(name, shape, B, T)
-        entry = {"name": name, "ms_per_step": tot / args.profile_steps,
+        entry = {"name": name, "ms_per_step": tot / args.steps,
                  "share": tot / prof_total}
         if kind == "tensor":
             entry["tflops"] = amount * cnt / (tot / 1000.0) / 1e12
@@ -376,7 +404,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="d20_bf16", choices=sorted(nc_synth.WORKLOADS))
-    ap.add_argument("--profile-steps", type=int, default=2)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -8,10 +8,12 @@
 // packed rows meets a single K/V tile and every K/V byte brought on chip
 // serves all H heads; key j is visible to packed row r iff j <= r / H.
 //
-// Every kernel is warp-specialised (256 threads): warp 0 issues TMA, warp 1
-// issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..7 are the
-// softmax warps -- thread i of them owns TMEM lane i, i.e. one row of the
-// score tile, so row reductions need no shuffles.  Probabilities go from
+// Every kernel is warp-specialised (384 threads): warp 0 issues TMA, warp 1
+// issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..11 are two
+// softmax warpgroups -- a thread owns one TMEM lane, i.e. one row of the
+// score tile, and half of its columns (the other half belongs to the thread
+// of the same lane in the other warpgroup), so row reductions need no
+// shuffles and two warps per scheduler hide each other's latency.  Probabilities go from
 // registers to 128B-swizzled shared memory as the next MMA's operand.  A
 // 64-wide [row][64 dims] swizzled tile is both a K-major operand (rows = N)
 // and an MN-major one (rows = K), so no operand is ever transposed.  All
@@ -29,7 +31,8 @@ namespace {
 using namespace tc;
 
 constexpr int HD = 128;
-constexpr int NT = 256;  // threads per CTA
+constexpr int NT = 384;  // threads per CTA: 4 control warps + 2 softmax warpgroups
+constexpr int NSW = 8;   // softmax warps (warps 4..11); warp w reads TMEM lanes 32 (w % 4) ..
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int SITE_ATTN = 300;
@@ -51,6 +54,29 @@ __device__ __forceinline__ void store_row_atom(uint8_t* atom, int row, const flo
     q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
     *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = q;
   }
+}
+
+// Store 32 bf16 values (one half of a 64-wide row) into a [rows][64]
+// 128B-swizzled atom: 16-byte chunks chunk0 .. chunk0 + 3 of the row.
+__device__ __forceinline__ void store_half_row_atom(uint8_t* atom, int row, int chunk0,
+                                                    const float* x) {
+  uint8_t* base = atom + row * 128;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint4 q;
+    q.x = pack2(x[ch * 8 + 0], x[ch * 8 + 1]);
+    q.y = pack2(x[ch * 8 + 2], x[ch * 8 + 3]);
+    q.z = pack2(x[ch * 8 + 4], x[ch * 8 + 5]);
+    q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
+    *reinterpret_cast<uint4*>(base + (((chunk0 + ch) ^ (row & 7)) << 4)) = q;
+  }
+}
+
+// 2^x on the special-function unit (approximate, flushes denormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // Store 32 fp32 values as bf16 to global (64 contiguous bytes).
@@ -85,7 +111,9 @@ constexpr int Q_OFF = 0;                    // 32 KB
 constexpr int K_OFF = 32768;                // 2 x 32 KB
 constexpr int V_OFF = K_OFF + 2 * 32768;    // 2 x 32 KB
 constexpr int P_OFF = V_OFF + 2 * 32768;    // 32 KB
-constexpr int BAR_OFF = P_OFF + 32768;
+constexpr int RED_OFF = P_OFF + 32768;      // [2 parity][2 half][128] row maxima
+constexpr int LSUM_OFF = RED_OFF + 2048;    // [2 half][128] row sums
+constexpr int BAR_OFF = LSUM_OFF + 1024;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 }  // namespace fwd
 
@@ -105,18 +133,20 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* v_full = bars + 5;   // [2]
   uint64_t* v_empty = bars + 7;  // [2]
   uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2], 128 arrivals
-  uint64_t* p_full = bars + 13;  // 128 arrivals
+  uint64_t* s_free = bars + 11;  // [2], one arrival per softmax warp
+  uint64_t* p_full = bars + 13;  // one arrival per softmax warp
   uint64_t* o_done = bars + 14;
   uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* red_full = bars + 16;  // [2], one arrival per softmax warp
+  uint64_t* lsum_full = bars + 18; // one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
+  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
   const long TH = (long)T * H;
   const int n_qt = (int)((TH + BQ - 1) / BQ);
-  const long r0 = (long)(n_qt - 1 - blockIdx.x) * BQ;  // heaviest tiles first
+  const long r0 = (long)(n_qt - 1 - blockIdx.y) * BQ;  // heaviest tiles first
   const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
   const int nkv = t_last / BKV + 1;
 
@@ -128,11 +158,14 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&s_free[i], NSW);
     }
-    mbar_init(p_full, 128);
+    mbar_init(p_full, NSW);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(&red_full[0], NSW);
+    mbar_init(&red_full[1], NSW);
+    mbar_init(lsum_full, NSW);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -217,40 +250,54 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax / epilogue
+    // Warp 4 + 4 half + quarter owns packed rows 32 quarter .. 32 quarter + 31
+    // (its TMEM lanes) and key columns 64 half .. 64 half + 63 of each tile;
+    // the two halves of a row exchange their maxima through shared memory.
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
     const long r = r0 + row;
     const bool valid = r < TH;
     const int t = (int)(r / H);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
-    float m_run = -INFINITY, l_run = 0.f;
+    float* red = reinterpret_cast<float*>(smem + RED_OFF);
+    float* lsum = reinterpret_cast<float*>(smem + LSUM_OFF);
+    const int t0 = (int)(r0 / H);
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's columns only
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
       tc_fence_after();
-      float s[BKV];
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        tmem_ld_32cols(tmem + lane_off + st * BKV + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-      }
+      float s[64];
+      tmem_ld_32cols(tmem + lane_off + st * BKV + half * 64, *reinterpret_cast<float(*)[32]>(s));
+      tmem_ld_32cols(tmem + lane_off + st * BKV + half * 64 + 32,
+                     *reinterpret_cast<float(*)[32]>(s + 32));
       tc_fence_before();
-      mbar_arrive(&s_free[st]);
-      const int key0 = j * BKV;
-      const bool need_mask = key0 + BKV - 1 > t || key0 + BKV > T;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[st]);
+      const int key0 = j * BKV + half * 64;
+      // Keys past every row's token (or past the sequence) occur only in
+      // tiles reaching beyond t0, the first row's token.
+      const bool need_mask = key0 + 63 > t0;
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
+      for (int i = 0; i < 64; ++i) {
         float x = s[i] * sl2;
         if (need_mask && (key0 + i > t || key0 + i >= T)) x = -INFINITY;
         s[i] = x;
         mx = fmaxf(mx, x);
       }
+      // Exchange the halves' maxima (buffers alternate by tile parity, so a
+      // fast warp never overwrites values a slow one has yet to read).
+      float* rp = red + (j & 1) * 256;
+      rp[half * 128 + row] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_full[j & 1]);
+      if (!sync.wait(&red_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+      mx = fmaxf(rp[row], rp[128 + row]);
       // PV of the previous tile must be done before O is rescaled and before
       // the single P buffer is overwritten.
       if (j > 0) {
@@ -258,15 +305,16 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
       }
       if (mx > m_run + 8.f) {
-        const float alpha = exp2f(m_run - mx);  // 0 on the first tile
+        const float alpha = ex2(m_run - mx);  // 0 on the first tile
         if (j > 0) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t oc = tmem + lane_off + 256 + half * 64 + c * 32;
             float v[32];
-            tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
+            tmem_ld_32cols(oc, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st_32cols(tmem + lane_off + 256 + c * 32, v);
+            tmem_st_32cols(oc, v);
           }
         }
         l_run *= alpha;
@@ -274,29 +322,34 @@ __global__ void __launch_bounds__(NT, 1)
       }
       float ls = 0.f;
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        const float p = exp2f(s[i] - m_run);
+      for (int i = 0; i < 64; ++i) {
+        const float p = ex2(s[i] - m_run);
         s[i] = p;
         ls += p;
       }
       l_run += ls;
-      store_row_atom(smem + P_OFF, row, s);
-      store_row_atom(smem + P_OFF + ATOM, row, s + 64);
+      store_row_atom(smem + P_OFF + half * ATOM, row, s);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
     }
+    lsum[half * 128 + row] = l_run;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(lsum_full);
+    if (ok) ok = sync.wait(lsum_full, 0);
+    const float l_tot = lsum[row] + lsum[128 + row];
     if (ok && sync.wait(o_done, (nkv - 1) & 1)) {
       tc_fence_after();
-      const float inv = 1.f / l_run;
+      const float inv = 1.f / l_tot;
       bf16* orow = o + ((long)b * TH + r) * HD;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         float v[32];
         tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
         if (valid) store_bf16_32(orow + c * 32, v, inv);
       }
-      if (valid) lse[(long)b * TH + r] = (m_run + log2f(l_run)) * kLn2;
+      if (valid && half == 0) lse[(long)b * TH + r] = (m_run + log2f(l_tot)) * kLn2;
     }
   }
   tc_fence_before();
@@ -320,7 +373,8 @@ constexpr int DO_OFF = 32768;                // 32 KB
 constexpr int K_OFF = 65536;                 // 2 x 16 KB
 constexpr int V_OFF = K_OFF + 2 * 16384;     // 2 x 16 KB
 constexpr int DS_OFF = V_OFF + 2 * 16384;    // 16 KB ([128 rows][64 keys])
-constexpr int BAR_OFF = DS_OFF + 16384;
+constexpr int DL_OFF = DS_OFF + 16384;       // [2][128] fp32 halves of delta
+constexpr int BAR_OFF = DL_OFF + 1024;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 }  // namespace bdq
 
@@ -341,18 +395,18 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* kv_full = bars + 1;   // [2]
   uint64_t* kv_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_free = bars + 7;    // [2], 128 arrivals
-  uint64_t* ds_full = bars + 9;   // 128 arrivals
+  uint64_t* s_free = bars + 7;    // [2], one arrival per softmax warp
+  uint64_t* ds_full = bars + 9;   // one arrival per softmax warp
   uint64_t* dq_done = bars + 10;
   uint64_t* drain = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
+  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
   const long TH = (long)T * H;
   const int n_qt = (int)((TH + BQ - 1) / BQ);
-  const long r0 = (long)(n_qt - 1 - blockIdx.x) * BQ;
+  const long r0 = (long)(n_qt - 1 - blockIdx.y) * BQ;
   const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
   const int nkv = t_last / BKV + 1;
 
@@ -362,9 +416,9 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&s_free[i], NSW);
     }
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, NSW);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -451,7 +505,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
+    // Softmax warps: warp 4 + 4 half + quarter owns packed rows 32 quarter ..
+    // 32 quarter + 31 (its TMEM lanes) and key columns 32 half .. 32 half + 31.
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
     const long r = r0 + row;
     const bool valid = r < TH;
@@ -459,12 +516,14 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
     const long grow = (long)b * TH + r;
+    // delta = rowsum(dO * O): each half sums 64 of the 128 dims.
+    float* dl_part = reinterpret_cast<float*>(smem + DL_OFF);
     float dl = 0.f, lse2 = 0.f;
     if (valid) {
-      const bf16* orow = o + grow * HD;
-      const bf16* drow = dout + grow * HD;
+      const bf16* orow = o + grow * HD + half * 64;
+      const bf16* drow = dout + grow * HD + half * 64;
 #pragma unroll 4
-      for (int i = 0; i < HD; i += 8) {
+      for (int i = 0; i < 64; i += 8) {
         const uint4 a = *reinterpret_cast<const uint4*>(orow + i);
         const uint4 d = *reinterpret_cast<const uint4*>(drow + i);
         const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -475,49 +534,51 @@ __global__ void __launch_bounds__(NT, 1)
           dl += fa.x * fd.x + fa.y * fd.y;
         }
       }
-      delta[grow] = dl;
       lse2 = lse[grow] * kLog2e;
     }
+    dl_part[half * 128 + row] = dl;
+    asm volatile("bar.sync 1, %0;" ::"n"(NSW * 32) : "memory");  // the 8 softmax warps
+    dl = dl_part[row] + dl_part[128 + row];
+    if (valid && half == 0) delta[grow] = dl;
+    // Rows of this CTA hold tokens t0 .. t_last; a key tile needs the mask
+    // only where it reaches past t0 (or the tile has rows past the sequence).
+    const int t0 = (int)(r0 / H);
+    const bool rows_ragged = r0 + BQ > TH;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
       tc_fence_after();
-      float s[BKV], dp[BKV];
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        tmem_ld_32cols(tmem + lane_off + st * 64 + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-        tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dp[c * 32 + i] = v[i];
-      }
+      float s[32], dp[32];
+      tmem_ld_32cols(tmem + lane_off + st * 64 + half * 32, s);
+      tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + half * 32, dp);
       tc_fence_before();
-      mbar_arrive(&s_free[st]);
-      const int key0 = j * BKV;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[st]);
+      const int key0 = j * BKV + half * 32;
+      const bool need_mask = rows_ragged || key0 + 31 > t0;
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        float p = exp2f(s[i] * sl2 - lse2);
-        if (!valid || key0 + i > t || key0 + i >= T) p = 0.f;
+      for (int i = 0; i < 32; ++i) {
+        float p = ex2(fmaf(s[i], sl2, -lse2));
+        if (need_mask && (!valid || key0 + i > t)) p = 0.f;
         s[i] = p * (dp[i] - dl);
       }
       if (j > 0) {  // the dQ MMA of the previous tile has read the dS buffer
         if (!sync.wait(dq_done, (j - 1) & 1)) { ok = false; break; }
       }
-      store_row_atom(smem + DS_OFF, row, s);
+      store_half_row_atom(smem + DS_OFF, row, half * 4, s);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
     }
     if (ok && sync.wait(dq_done, (nkv - 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       bf16* qrow = dq + ((long)b * T + t) * ldq + (long)(r % H) * HD;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         float v[32];
         tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
         if (valid) store_bf16_32(qrow + c * 32, v, scale);
@@ -568,12 +629,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* q_full = bars + 1;   // [2]
   uint64_t* q_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2], 128 arrivals
-  uint64_t* p_full = bars + 9;   // 128 arrivals
+  uint64_t* s_free = bars + 7;   // [2], one arrival per softmax warp
+  uint64_t* p_full = bars + 9;   // one arrival per softmax warp
   uint64_t* pd_done = bars + 10;
   uint64_t* drain = bars + 11;
   uint64_t* info_full = bars + 12;  // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 14;  // [2], 128 arrivals
+  uint64_t* info_free = bars + 14;  // [2], one arrival per softmax warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][64]
@@ -581,8 +642,8 @@ __global__ void __launch_bounds__(NT, 1)
   int* info_tok = reinterpret_cast<int*>(info_dl + 2 * 64);           // [2][64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
-  const int j0 = blockIdx.x * BKV;
+  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
+  const int j0 = blockIdx.y * BKV;  // heaviest (earliest keys) first
   const long TH = (long)T * H;
   const long rt0 = ((long)j0 * H) / BQ;
   const int n_rt = (int)((TH + BQ - 1) / BQ - rt0);
@@ -593,14 +654,14 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&s_free[i], NSW);
     }
-    mbar_init(p_full, 128);
+    mbar_init(p_full, NSW);
     mbar_init(pd_done, 1);
     mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&info_full[i], 32);
-      mbar_init(&info_free[i], 128);
+      mbar_init(&info_free[i], NSW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -709,7 +770,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
+    // Softmax warps: warp 4 + 4 half + quarter owns key rows 32 quarter ..
+    // 32 quarter + 31 (its TMEM lanes) and query columns 32 half .. 32 half + 31.
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int krow = quarter * 32 + lane;  // key inside the tile
     const int key = j0 + krow;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -720,35 +784,45 @@ __global__ void __launch_bounds__(NT, 1)
       const uint32_t ph = (i >> 1) & 1;
       if (!sync.wait(&s_full[st], ph) || !sync.wait(&info_full[st], ph)) { ok = false; break; }
       tc_fence_after();
-      float s[BQ], dp[BQ];
-#pragma unroll
-      for (int c = 0; c < BQ / 32; ++c) {
-        float v[32];
-        tmem_ld_32cols(tmem + lane_off + st * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[c * 32 + k] = v[k];
-        tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[c * 32 + k] = v[k];
-      }
+      float s[32], dp[32];
+      tmem_ld_32cols(tmem + lane_off + st * 64 + half * 32, s);
+      tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + half * 32, dp);
       tc_fence_before();
-      mbar_arrive(&s_free[st]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[st]);
+      const float* il = info_lse + st * 64 + half * 32;
+      const float* id = info_dl + st * 64 + half * 32;
+      const int* it = info_tok + st * 64 + half * 32;
+      // Rows are in token order, so it[0] is the smallest token of these 32
+      // rows; rows past the sequence carry token -1.  Only tiles that cross
+      // the diagonal (or the end) need the mask.
+      const bool need_mask = j0 + BKV - 1 > it[0] || it[31] < 0;
 #pragma unroll
-      for (int c = 0; c < BQ; ++c) {
-        float p = exp2f(s[c] * sl2 - info_lse[st * 64 + c]);
-        if (key > info_tok[st * 64 + c] || key >= T) p = 0.f;
-        s[c] = p;
-        dp[c] = p * (dp[c] - info_dl[st * 64 + c]);
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l4 = reinterpret_cast<const float4*>(il)[c4];
+        const float4 d4 = reinterpret_cast<const float4*>(id)[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c4 * 4 + e;
+          float p = ex2(fmaf(s[c], sl2, -lv[e]));
+          if (need_mask && key > it[c]) p = 0.f;
+          s[c] = p;
+          dp[c] = p * (dp[c] - dv4[e]);
+        }
       }
-      mbar_arrive(&info_free[st]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&info_free[st]);
       if (i > 0) {  // dV/dK MMAs of the previous tile have read P^T, dS^T
         if (!sync.wait(pd_done, (i - 1) & 1)) { ok = false; break; }
       }
-      store_row_atom(smem + PT_OFF, krow, s);
-      store_row_atom(smem + DST_OFF, krow, dp);
+      store_half_row_atom(smem + PT_OFF, krow, half * 4, s);
+      store_half_row_atom(smem + DST_OFF, krow, half * 4, dp);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
     }
     if (ok && n_rt > 0 && sync.wait(pd_done, (n_rt - 1) & 1)) {
       tc_fence_after();
@@ -756,7 +830,7 @@ __global__ void __launch_bounds__(NT, 1)
       const bool valid = key < T;
       const long tok = (long)b * T + key;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         float v[32];
         tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
         if (valid) store_bf16_32(dv + tok * ldv + c * 32, v, 1.f);
@@ -802,7 +876,7 @@ cudaError_t attention_fwd_tc(int B, int T, int H, const void* q, const void* k, 
   if (!map3(&mq, q, TH, B, fwd::BQ) || !map3(&mk, k, T, B, fwd::BKV) ||
       !map3(&mv, v, T, B, fwd::BKV))
     return cudaErrorInvalidValue;
-  dim3 grid((unsigned)((TH + fwd::BQ - 1) / fwd::BQ), B);
+  dim3 grid(B, (unsigned)((TH + fwd::BQ - 1) / fwd::BQ));
   attn_fwd_tc_kernel<<<grid, NT, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, T, H,
                                                           ctx.err, ctx.timeout_ns);
   return launched(1);
@@ -824,7 +898,7 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   if (!map3(&mq, q, TH, B, bdq::BQ) || !map3(&mdo, dout, TH, B, bdq::BQ) ||
       !map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV))
     return cudaErrorInvalidValue;
-  dim3 gq((unsigned)((TH + bdq::BQ - 1) / bdq::BQ), B);
+  dim3 gq(B, (unsigned)((TH + bdq::BQ - 1) / bdq::BQ));
   attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
       mq, mdo, mk, mv, (const nc::bf16*)o, (const nc::bf16*)dout, lse, (nc::bf16*)dq, ldq, delta,
       T, H, ctx.err, ctx.timeout_ns);
@@ -834,7 +908,7 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ) ||
       !map3(&mk, k, T, B, bkv::BKV) || !map3(&mv, v, T, B, bkv::BKV))
     return cudaErrorInvalidValue;
-  dim3 gk((unsigned)((T + bkv::BKV - 1) / bkv::BKV), B);
+  dim3 gk(B, (unsigned)((T + bkv::BKV - 1) / bkv::BKV));
   attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(mq, mdo, mk, mv, lse, delta,
                                                              (nc::bf16*)dk, ldk, (nc::bf16*)dv,
                                                              ldv, T, H, ctx.err, ctx.timeout_ns);

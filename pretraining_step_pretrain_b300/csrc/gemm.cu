@@ -111,9 +111,9 @@ cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx) {
 // ===================================================================
 namespace {
 
-// Work-unit count the split heuristic aims at (B300: 148 SMs).  The launch
-// itself uses the real SM count.
-constexpr int kSplitSms = 148;
+// Work-unit count the split heuristic aims at (B300: 148 SMs = 74 CTA pairs).
+// The launch itself uses the real SM count.
+constexpr int kSplitUnits = 74;
 
 struct Plan {
   tc::Sched sch;
@@ -128,7 +128,7 @@ Plan make_plan(int layout, int epi, int M, int N, int K, int group_m) {
   s.splits = 1;
   s.kb_per_split = s.k_blocks;
   const int tiles = s.m_tiles * s.n_tiles;
-  if (epi == EPI_STORE_F32 && tiles < 2 * kSplitSms && s.k_blocks >= 32) {
+  if (epi == EPI_STORE_F32 && tiles < 2 * kSplitUnits && s.k_blocks >= 32) {
     // Split the reduction so that the units fill the SMs; cost proxy =
     // waves x k-blocks per unit, plus one k-block per split for the slab pass.
     long best = -1;
@@ -137,7 +137,7 @@ Plan make_plan(int layout, int epi, int M, int N, int K, int group_m) {
       if (kbp < 8) break;
       const int eff_splits = (s.k_blocks + kbp - 1) / kbp;
       const int units = tiles * eff_splits;
-      const long waves = (units + kSplitSms - 1) / kSplitSms;
+      const long waves = (units + kSplitUnits - 1) / kSplitUnits;
       const long cost = waves * kbp + (eff_splits > 1 ? eff_splits : 0);
       if (best < 0 || cost < best) {
         best = cost;
@@ -186,9 +186,9 @@ template <bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ctx& ctx) {
   CUtensorMap ta, tb;
   bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
-                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, tc::BM);
+                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, tc::HALF_ROWS);
   ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
-                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::BN));
+                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::HALF_ROWS));
   if (!ok) return cudaErrorInvalidValue;
   auto kern = tc::gemm_bf16_tc_kernel<A_MN, B_MN, Epi>;
   static bool attr_set = false;  // per instantiation
@@ -198,7 +198,8 @@ cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ct
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = std::min(p.sch.units, ctx.num_sms);
+  // One CTA pair (a 2-CTA cluster) per unit, at most one CTA per SM.
+  const int grid = 2 * std::max(1, std::min(p.sch.units, ctx.num_sms / 2));
   kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, ctx.stream>>>(ta, tb, p.sch, g.M, g.N, epi, ctx.err,
                                                              ctx.timeout_ns);
   return launched(1);

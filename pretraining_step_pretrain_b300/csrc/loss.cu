@@ -109,31 +109,71 @@ __global__ void ce_loss_kernel(const float* __restrict__ lse, const float* __res
   }
 }
 
-// dz in place.  TS: stored capped logit type, TG: gradient type written over it.
+// 8 consecutive elements: one 16-byte access for 16-bit types, two for fp32.
+__device__ __forceinline__ void load8(const __half* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  Vec4<float>::load(p, *reinterpret_cast<float(*)[4]>(v));
+  Vec4<float>::load(p + 4, *reinterpret_cast<float(*)[4]>(v + 4));
+}
+__device__ __forceinline__ void store8(bf16* p, const float (&v)[8]) {
+  uint4 q;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(p) = q;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  Vec4<float>::store(p, *reinterpret_cast<const float(*)[4]>(v));
+  Vec4<float>::store(p + 4, *reinterpret_cast<const float(*)[4]>(v + 4));
+}
+
+// dz in place.  TS: stored capped logit type, TG: gradient type written over
+// it (same size).  One CTA per row; 8 elements (16 B of fp16/bf16, two 16 B
+// vectors of fp32) per thread and step.
 template <typename TS, typename TG, bool kFastExp>
-__global__ void ce_dlogits_kernel(TS* __restrict__ s, const float* __restrict__ lse,
-                                  const int* __restrict__ targets, const float* __restrict__ inv_n,
-                                  int M, int V, float cap) {
-  const long n4 = (long)M * V / 4;
-  const float scale = *inv_n;
+__global__ void __launch_bounds__(256) ce_dlogits_kernel(TS* __restrict__ s,
+                                                         const float* __restrict__ lse,
+                                                         const int* __restrict__ targets,
+                                                         const float* __restrict__ inv_n, int V,
+                                                         float cap) {
+  const long row = blockIdx.x;
+  int y = targets[row];
+  if (y >= V) y = -1;
+  const float scale = y >= 0 ? *inv_n : 0.f;  // ignored rows get a zero gradient
   const float inv_c = 1.f / cap;
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4;
-       i += (long)gridDim.x * blockDim.x) {
-    const long e0 = 4 * i;
-    const int row = (int)(e0 / V), col = (int)(e0 % V);
-    int y = targets[row];
-    if (y >= V) y = -1;
-    float v[4];
-    Vec4<TS>::load(s + e0, v);
-    const float l = lse[row];
-    for (int k = 0; k < 4; ++k) {
+  const float l = lse[row];
+  TS* sr = s + row * V;
+  TG* gr = reinterpret_cast<TG*>(sr);
+  const int v8 = V & ~7;
+  for (int c = threadIdx.x * 8; c < v8; c += blockDim.x * 8) {
+    float v[8];
+    load8(sr + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
       const float sv = v[k];
       const float p = kFastExp ? __expf(sv - l) : expf(sv - l);
       const float t = sv * inv_c;
-      float g = (p - (col + k == y ? 1.f : 0.f)) * (1.f - t * t) * scale;
-      v[k] = y >= 0 ? g : 0.f;
+      v[k] = (p - (c + k == y ? 1.f : 0.f)) * (1.f - t * t) * scale;
     }
-    Vec4<TG>::store(reinterpret_cast<TG*>(s) + e0, v);
+    store8(gr + c, v);
+  }
+  for (int c = v8 + threadIdx.x; c < V; c += blockDim.x) {
+    const float sv = to_f(sr[c]);
+    const float p = kFastExp ? __expf(sv - l) : expf(sv - l);
+    const float t = sv * inv_c;
+    gr[c] = from_f<TG>((p - (c == y ? 1.f : 0.f)) * (1.f - t * t) * scale);
   }
 }
 
@@ -159,14 +199,13 @@ cudaError_t ce_loss(const float* lse, const float* s_tgt, const int* targets, in
 
 cudaError_t ce_dlogits(bool bf16, void* s, const float* lse, const int* targets,
                        const float* inv_n, int M, int V, float cap, const Ctx& ctx) {
-  const long n4 = (long)M * V / 4;
-  const int blocks = (int)std::max<long>(1, std::min<long>((n4 + 255) / 256, (long)ctx.num_sms * 32));
+  if (M <= 0) return cudaSuccess;
   if (bf16)
-    ce_dlogits_kernel<__half, nc::bf16, true><<<blocks, 256, 0, ctx.stream>>>(
-        static_cast<__half*>(s), lse, targets, inv_n, M, V, cap);
+    ce_dlogits_kernel<__half, nc::bf16, true><<<M, 256, 0, ctx.stream>>>(
+        static_cast<__half*>(s), lse, targets, inv_n, V, cap);
   else
-    ce_dlogits_kernel<float, float, false><<<blocks, 256, 0, ctx.stream>>>(
-        static_cast<float*>(s), lse, targets, inv_n, M, V, cap);
+    ce_dlogits_kernel<float, float, false><<<M, 256, 0, ctx.stream>>>(
+        static_cast<float*>(s), lse, targets, inv_n, V, cap);
   return launched(1);
 }
 

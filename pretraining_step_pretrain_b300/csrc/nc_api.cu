@@ -87,6 +87,9 @@ nc_status check_cfg(const nc_config* c, int B, int T) {
     return fail(NC_ERR_UNSUPPORTED_SHAPE, "vocab %d must be a multiple of 64 in [64, 2^24]", c->vocab);
   if (B < 1 || T < 1 || (long)B * T > (1L << 24))
     return fail(NC_ERR_UNSUPPORTED_SHAPE, "B=%d T=%d: need B, T >= 1 and B*T <= 2^24", B, T);
+  if ((long)T * c->n_head > kMaxAttnRowsPerSeq)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "T*n_head = %ld exceeds %ld query rows per sequence",
+                (long)T * c->n_head, kMaxAttnRowsPerSeq);
   if (!(c->softcap > 0.f) || !(c->eps >= 0.f) || !(c->rope_base > 0.f))
     return fail(NC_ERR_INVALID_ARG, "softcap, rope_base must be > 0 and eps >= 0");
   return NC_OK;
@@ -620,6 +623,9 @@ static nc_status check_attn(int dtype, int B, int T, int H, int h) {
   if (dtype != NC_BF16 && dtype != NC_F32) return fail(NC_ERR_INVALID_ARG, "bad dtype %d", dtype);
   if (B < 1 || T < 1 || H < 1 || (long)B * T * H > (1L << 28))
     return fail(NC_ERR_UNSUPPORTED_SHAPE, "bad B/T/H");
+  if ((long)T * H > kMaxAttnRowsPerSeq)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "T*H = %ld exceeds %ld query rows per sequence",
+                (long)T * H, kMaxAttnRowsPerSeq);
   if (h != 128 && !(dtype == NC_F32 && h == 64))
     return fail(NC_ERR_UNSUPPORTED_SHAPE, "head_dim %d unsupported for this dtype", h);
   return NC_OK;

@@ -22,6 +22,11 @@ inline cudaError_t launched(int n) {
   return cudaGetLastError();
 }
 
+// Query rows (tokens x heads) of one sequence that the attention kernels
+// accept: their tiles are indexed by the grid's y dimension (<= 65535 tiles
+// of 128 rows).
+constexpr long kMaxAttnRowsPerSeq = 65535L * 128;
+
 enum GemmLayout { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_ADD_F32 = 2, EPI_RELU2 = 3,
                EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5 };

@@ -19,6 +19,26 @@ __device__ __forceinline__ float rms_inv(float sumsq, int n, float eps) {
   return rsqrtf(sumsq / (float)n + eps);
 }
 
+// E consecutive elements (E = 4: one 8- or 16-byte access; E = 2: scalars).
+template <typename A, int E>
+__device__ __forceinline__ void load_vec(const A* p, float (&x)[E]) {
+  if constexpr (E == 4) {
+    Vec4<A>::load(p, x);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = to_f(p[e]);
+  }
+}
+template <typename A, int E>
+__device__ __forceinline__ void store_vec(A* p, const float (&x)[E]) {
+  if constexpr (E == 4) {
+    Vec4<A>::store(p, x);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) p[e] = from_f<A>(x[e]);
+  }
+}
+
 // ---- RoPE table: tab[t * h/2 + i] = (cos, sin)(t * base^(-2i/h)), fp64 math.
 __global__ void rope_table_kernel(float2* tab, int T, int half, int h, double base) {
   const long n = (long)T * half;
@@ -151,45 +171,49 @@ __global__ void qknorm_rope_fwd_kernel(const A* __restrict__ qkv, const float2* 
                                        A* __restrict__ q, A* __restrict__ k, A* __restrict__ v,
                                        float* __restrict__ rstd_qk, int M, int T, int H,
                                        float eps) {
+  // One warp per token: H query heads, the key head, the value head.  The
+  // token's (cos, sin) pairs are read once; four heads are loaded before any
+  // is used so that several loads are in flight per lane.
   constexpr int h = 32 * E, half = h / 2;
-  const long item = blockIdx.x * (long)kWarpsPerBlock + (threadIdx.x >> 5);
+  const int m = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (item >= (long)M * (H + 2)) return;
-  const int m = (int)(item / (H + 2)), j = (int)(item % (H + 2));
-  const A* src = qkv + (long)m * (H + 2) * h + (long)j * h + lane * E;
-  float x[E];
-  if (E == 4) {
-    float t[4];
-    Vec4<A>::load(src, t);
-    for (int e = 0; e < E; ++e) x[e] = t[e];
-  } else {
-    for (int e = 0; e < E; ++e) x[e] = to_f(src[e]);
-  }
-  if (j == H + 1) {
-    A* dst = v + (long)m * h + lane * E;
-    for (int e = 0; e < E; ++e) dst[e] = from_f<A>(x[e]);
-    return;
-  }
-  float ss = 0.f;
-  for (int e = 0; e < E; ++e) ss += x[e] * x[e];
-  const float r = rms_inv(warp_sum(ss), h, eps);
+  if (m >= M) return;
   const int t = m % T;
   const bool lo = lane < 16;
-  float out[E];
-  for (int e = 0; e < E; ++e) {
-    const float y = x[e] * r;
-    const float p = __shfl_xor_sync(0xffffffffu, y, 16);
-    const float2 cs = tab[(long)t * half + (lane & 15) * E + e];
-    out[e] = lo ? (y * cs.x - p * cs.y) : (p * cs.y + y * cs.x);
+  float2 cs[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) cs[e] = tab[(long)t * half + (lane & 15) * E + e];
+  const int nh = H + 2;
+  const A* src = qkv + (long)m * nh * h + lane * E;
+  for (int j0 = 0; j0 < nh; j0 += 4) {
+    float x[4][E];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u < nh) load_vec<A, E>(src + (long)(j0 + u) * h, x[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j >= nh) break;
+      if (j == H + 1) {
+        store_vec<A, E>(v + (long)m * h + lane * E, x[u]);
+        continue;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss += x[u][e] * x[u][e];
+      const float r = rms_inv(warp_sum(ss), h, eps);
+      float out[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float y = x[u][e] * r;
+        const float pr = __shfl_xor_sync(0xffffffffu, y, 16);
+        out[e] = lo ? (y * cs[e].x - pr * cs[e].y) : (pr * cs[e].y + y * cs[e].x);
+      }
+      A* dst = (j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E;
+      store_vec<A, E>(dst, out);
+      if (lane == 0) rstd_qk[(long)m * (H + 1) + j] = r;
+    }
   }
-  A* dst = (j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E;
-  if (E == 4) {
-    float t4[4] = {out[0], out[1], out[2], out[3]};
-    Vec4<A>::store(dst, t4);
-  } else {
-    for (int e = 0; e < E; ++e) dst[e] = from_f<A>(out[e]);
-  }
-  if (lane == 0) rstd_qk[(long)m * (H + 1) + j] = r;
 }
 
 // ---- QK-norm + RoPE backward, in place on the (M, (H+2)h) gradient buffer.
@@ -199,30 +223,48 @@ template <typename A, int E>
 __global__ void qknorm_rope_bwd_kernel(A* __restrict__ dqkv, const A* __restrict__ q,
                                        const A* __restrict__ k, const float* __restrict__ rstd_qk,
                                        const float2* __restrict__ tab, int M, int T, int H) {
+  // One warp per token (H query heads + the key head; the value gradient
+  // passes through), four heads' loads in flight before any is used.
   constexpr int h = 32 * E, half = h / 2;
-  const long item = blockIdx.x * (long)kWarpsPerBlock + (threadIdx.x >> 5);
+  const int m = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (item >= (long)M * (H + 1)) return;
-  const int m = (int)(item / (H + 1)), j = (int)(item % (H + 1));
-  A* gp = dqkv + (long)m * (H + 2) * h + (long)j * h + lane * E;
-  const A* zp = (j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E;
-  float g[E], z[E];
-  for (int e = 0; e < E; ++e) {
-    g[e] = to_f(gp[e]);
-    z[e] = to_f(zp[e]);
-  }
-  float dot = 0.f;
-  for (int e = 0; e < E; ++e) dot += g[e] * z[e];
-  const float mean = warp_sum(dot) / (float)h;
-  const float r = rstd_qk[(long)m * (H + 1) + j];
+  if (m >= M) return;
   const int t = m % T;
   const bool lo = lane < 16;
-  for (int e = 0; e < E; ++e) {
-    const float w = g[e] - z[e] * mean;
-    const float p = __shfl_xor_sync(0xffffffffu, w, 16);
-    const float2 cs = tab[(long)t * half + (lane & 15) * E + e];
-    const float o = lo ? (w * cs.x + p * cs.y) : (w * cs.x - p * cs.y);
-    gp[e] = from_f<A>(r * o);
+  float2 cs[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) cs[e] = tab[(long)t * half + (lane & 15) * E + e];
+  const int nh = H + 1;
+  A* grow = dqkv + (long)m * (H + 2) * h + lane * E;
+  for (int j0 = 0; j0 < nh; j0 += 4) {
+    float g[4][E], z[4][E];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j < nh) {
+        load_vec<A, E>(grow + (long)j * h, g[u]);
+        load_vec<A, E>((j < H) ? q + ((long)m * H + j) * h + lane * E : k + (long)m * h + lane * E,
+                       z[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j >= nh) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot += g[u][e] * z[u][e];
+      const float mean = warp_sum(dot) / (float)h;
+      const float r = rstd_qk[(long)m * (H + 1) + j];
+      float out[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float w = g[u][e] - z[u][e] * mean;
+        const float pr = __shfl_xor_sync(0xffffffffu, w, 16);
+        out[e] = r * (lo ? (w * cs[e].x + pr * cs[e].y) : (w * cs[e].x - pr * cs[e].y));
+      }
+      store_vec<A, E>(grow + (long)j * h, out);
+    }
   }
 }
 
@@ -286,7 +328,7 @@ cudaError_t qknorm_rope_fwd(bool bf16, const void* qkv, const float2* tab, void*
                             void* v, float* rstd_qk, int B, int T, int H, int h, float eps,
                             const Ctx& ctx) {
   const int M = B * T;
-  const int blocks = row_blocks((long)M * (H + 2));
+  const int blocks = row_blocks(M);
 #define NC_QKF(TA, EE)                                                                      \
   qknorm_rope_fwd_kernel<TA, EE><<<blocks, 32 * kWarpsPerBlock, 0, ctx.stream>>>(          \
       static_cast<const TA*>(qkv), tab, static_cast<TA*>(q), static_cast<TA*>(k),          \
@@ -304,7 +346,7 @@ cudaError_t qknorm_rope_bwd(bool bf16, void* dqkv, const void* q, const void* k,
                             const float* rstd_qk, const float2* tab, int B, int T, int H, int h,
                             const Ctx& ctx) {
   const int M = B * T;
-  const int blocks = row_blocks((long)M * (H + 1));
+  const int blocks = row_blocks(M);
 #define NC_QKB(TA, EE)                                                                      \
   qknorm_rope_bwd_kernel<TA, EE><<<blocks, 32 * kWarpsPerBlock, 0, ctx.stream>>>(          \
       static_cast<TA*>(dqkv), static_cast<const TA*>(q), static_cast<const TA*>(k), rstd_qk, \

@@ -80,6 +80,37 @@ def test_gemm_matches_torch(dtype, layout, epi, shape):
     assert err < (2e-5 if fp32_out and dtype == "f32" else 1e-4 if fp32_out else 8e-3), float(err)
 
 
+@pytest.mark.parametrize("layout", [nc.GEMM_NT, nc.GEMM_NN, nc.GEMM_TN], ids=["NT", "NN", "TN"])
+@pytest.mark.parametrize("epi", [nc.EPI_STORE, nc.EPI_ADD_F32, nc.EPI_RELU2_BWD],
+                         ids=["store", "add_f32", "relu2_bwd"])
+def test_gemm_many_tiles_per_cta_pair(layout, epi):
+    """More output tiles than CTA pairs (33 x 10 tiles of 256 x 256), so every
+    pair walks several tiles: both accumulators and every ring stage are
+    reused many times; ragged M and N edges."""
+    M, N, K = 8296, 2528, 320  # the API needs N % 32 == 0 and 16-byte row strides
+    gen = torch.Generator(device="cuda").manual_seed(layout * 5 + epi)
+    A, lda, B, ldb, ref = _operands(layout, M, N, K, torch.bfloat16, gen)
+    aux = None
+    if epi == nc.EPI_ADD_F32:
+        C = torch.randn(M, N, generator=gen, device="cuda")
+        expect = ref + C
+    elif epi == nc.EPI_RELU2_BWD:
+        C = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+        aux = torch.relu(torch.randn(M, N, generator=gen, device="cuda")).square().to(torch.bfloat16)
+        expect = ref * 2 * aux.float().sqrt()
+    else:
+        C = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+        expect = ref
+    nc.gemm(nc.NC_BF16, layout, epi, M, N, K, A, lda, B, ldb, C, N, aux=aux)
+    torch.cuda.synchronize()
+    err = float((C.float() - expect).norm() / expect.norm())
+    assert err < (1e-4 if epi == nc.EPI_ADD_F32 else 8e-3), err
+    # every tile was written (no tile skipped by the persistent walk)
+    assert bool(torch.isfinite(C.float()).all())
+    rows = (C.float() - expect).abs().amax(dim=1)
+    assert float(rows.max()) < 0.1 * float(expect.abs().max()), float(rows.max())
+
+
 @pytest.mark.parametrize("K", [8192, 65536])
 def test_gemm_split_k_weight_gradient(K):
     # dW-shaped: few output tiles, long reduction -> split-K with a fixed-order slab sum

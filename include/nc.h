@@ -49,7 +49,7 @@
  *
  * Shape limits: d_model % 64 == 0, head_dim in {64, 128} (128 only in
  * NC_BF16 mode), n_head >= 1, d_mlp % 64 == 0, vocab % 64 == 0,
- * vocab <= 2^24, B >= 1, T >= 1, B*T <= 2^24, T*n_head <= 65535*128.
+ * vocab <= 2^24, B >= 1, T >= 1, B*T <= 2^24, T*n_head <= 65534*128.
  */
 #ifndef NC_H
 #define NC_H

@@ -370,9 +370,10 @@ constexpr int QATOM = 16384;   // [128 rows][64]
 constexpr int KATOM = 8192;    // [64 keys][64]
 constexpr int Q_OFF = 0;                     // 32 KB
 constexpr int DO_OFF = 32768;                // 32 KB
-constexpr int K_OFF = 65536;                 // 2 x 16 KB
-constexpr int V_OFF = K_OFF + 2 * 16384;     // 2 x 16 KB
-constexpr int DS_OFF = V_OFF + 2 * 16384;    // 16 KB ([128 rows][64 keys])
+constexpr int KVS = 4;                       // K/V ring stages
+constexpr int K_OFF = 65536;                 // KVS x 16 KB
+constexpr int V_OFF = K_OFF + KVS * 16384;   // KVS x 16 KB
+constexpr int DS_OFF = V_OFF + KVS * 16384;  // 16 KB ([128 rows][64 keys])
 constexpr int DL_OFF = DS_OFF + 16384;       // [2][128] fp32 halves of delta
 constexpr int BAR_OFF = DL_OFF + 1024;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
@@ -392,14 +393,14 @@ __global__ void __launch_bounds__(NT, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_free = bars + 7;    // [2], one arrival per softmax warp
-  uint64_t* ds_full = bars + 9;   // one arrival per softmax warp
-  uint64_t* dq_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* kv_full = bars + 1;         // [KVS]
+  uint64_t* kv_empty = bars + 1 + KVS;  // [KVS]
+  uint64_t* s_full = bars + 1 + 2 * KVS;    // [2]
+  uint64_t* s_free = bars + 3 + 2 * KVS;    // [2], one arrival per softmax warp
+  uint64_t* ds_full = bars + 5 + 2 * KVS;   // one arrival per softmax warp
+  uint64_t* dq_done = bars + 6 + 2 * KVS;
+  uint64_t* drain = bars + 7 + 2 * KVS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * KVS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -412,9 +413,11 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < KVS; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], NSW);
     }
@@ -436,7 +439,8 @@ __global__ void __launch_bounds__(NT, 1)
   // TMEM columns: S[st] at 64 st, dP[st] at 128 + 64 st, dQ at 256.
 
   if (warp == 0 && lane == 0) {
-    int armed[3] = {-1, -1, -1};
+    int armed[1 + KVS];
+    for (int i = 0; i < 1 + KVS; ++i) armed[i] = -1;
     mbar_arrive_expect_tx(q_full, 4 * QATOM);
     tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, (int)r0, b);
     tma_load_3d(smem + Q_OFF + QATOM, &tmQ, q_full, 64, (int)r0, b);
@@ -444,21 +448,23 @@ __global__ void __launch_bounds__(NT, 1)
     tma_load_3d(smem + DO_OFF + QATOM, &tmDO, q_full, 64, (int)r0, b);
     armed[0] = 0;
     for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&kv_empty[st], ph ^ 1u)) break;
-      mbar_arrive_expect_tx(&kv_full[st], 4 * KATOM);
-      tma_load_3d(smem + K_OFF + st * 16384, &tmK, &kv_full[st], 0, j * BKV, b);
-      tma_load_3d(smem + K_OFF + st * 16384 + KATOM, &tmK, &kv_full[st], 64, j * BKV, b);
-      tma_load_3d(smem + V_OFF + st * 16384, &tmV, &kv_full[st], 0, j * BKV, b);
-      tma_load_3d(smem + V_OFF + st * 16384 + KATOM, &tmV, &kv_full[st], 64, j * BKV, b);
-      armed[1 + st] = (int)ph;
+      const int ks = j % KVS;
+      const uint32_t kph = (j / KVS) & 1;
+      if (!sync.wait(&kv_empty[ks], kph ^ 1u)) break;
+      mbar_arrive_expect_tx(&kv_full[ks], 4 * KATOM);
+      tma_load_3d(smem + K_OFF + ks * 16384, &tmK, &kv_full[ks], 0, j * BKV, b);
+      tma_load_3d(smem + K_OFF + ks * 16384 + KATOM, &tmK, &kv_full[ks], 64, j * BKV, b);
+      tma_load_3d(smem + V_OFF + ks * 16384, &tmV, &kv_full[ks], 0, j * BKV, b);
+      tma_load_3d(smem + V_OFF + ks * 16384 + KATOM, &tmV, &kv_full[ks], 64, j * BKV, b);
+      armed[1 + ks] = (int)kph;
     }
     if (*abort_flag) {
       int none = 0;
-      uint64_t* fb[3] = {q_full, &kv_full[0], &kv_full[1]};
-      for (int i = 0; i < 3; ++i)
-        if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
+      if (armed[0] >= 0) mbar_wait_bounded(q_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      for (int i = 0; i < KVS; ++i)
+        if (armed[1 + i] >= 0)
+          mbar_wait_bounded(&kv_full[i], (uint32_t)armed[1 + i], &none, err, SITE_ATTN,
+                            timeout_ns / 8);
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
@@ -467,12 +473,14 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t sDS = smem_u32(smem + DS_OFF);
     bool ok = sync.wait(q_full, 0), issued = false;
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;
+      const int st = j & 1;  // TMEM S / dP buffer
       const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&kv_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+      const int ks = j % KVS;  // shared-memory K/V stage
+      if (!sync.wait(&kv_full[ks], (j / KVS) & 1) || !sync.wait(&s_free[st], ph ^ 1u))
+        return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + st * 16384);
-      const uint32_t sV = smem_u32(smem + V_OFF + st * 16384);
+      const uint32_t sK = smem_u32(smem + K_OFF + ks * 16384);
+      const uint32_t sV = smem_u32(smem + V_OFF + ks * 16384);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
         umma_bf16(tmem + st * 64, desc_k_atoms(sQ, kk, QATOM), desc_k_atoms(sK, kk, KATOM), idS,
@@ -488,16 +496,16 @@ __global__ void __launch_bounds__(NT, 1)
     if (ok) ok = issue_s(0);
     for (int j = 0; ok && j < nkv; ++j) {
       if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-      const int st = j & 1;
+      const int ks = j % KVS;
       if (!sync.wait(ds_full, j & 1)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + st * 16384);
+      const uint32_t sK = smem_u32(smem + K_OFF + ks * 16384);
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk)
         umma_bf16(tmem + 256, desc_k_atoms(sDS, kk, QATOM), desc_mn_blocks(sK, kk, KATOM), idQ,
                   (j > 0 || kk > 0) ? 1u : 0u);
       umma_commit(dq_done);
-      umma_commit(&kv_empty[st]);
+      umma_commit(&kv_empty[ks]);
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
@@ -603,13 +611,15 @@ constexpr int KATOM = 16384;   // [128 keys][64]
 constexpr int QATOM = 8192;    // [64 rows][64]
 constexpr int K_OFF = 0;                      // 32 KB
 constexpr int V_OFF = 32768;                  // 32 KB
-constexpr int Q_OFF = 65536;                  // 2 x 16 KB
-constexpr int DO_OFF = Q_OFF + 2 * 16384;     // 2 x 16 KB
-constexpr int PT_OFF = DO_OFF + 2 * 16384;    // 16 KB ([128 keys][64 rows])
+constexpr int QS = 4;                         // Q / dO ring stages
+constexpr int Q_OFF = 65536;                  // QS x 16 KB
+constexpr int DO_OFF = Q_OFF + QS * 16384;    // QS x 16 KB
+constexpr int PT_OFF = DO_OFF + QS * 16384;   // 16 KB ([128 keys][64 rows])
 constexpr int DST_OFF = PT_OFF + 16384;       // 16 KB
 constexpr int INFO_OFF = DST_OFF + 16384;     // [2][64] x (lse2, delta, tok)
 constexpr int BAR_OFF = INFO_OFF + 2 * 64 * 12 + 128;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
+static_assert(SMEM <= 232448, "dK/dV pass shared memory exceeds 227 KB");
 }  // namespace bkv
 
 __global__ void __launch_bounds__(NT, 1)
@@ -626,16 +636,16 @@ __global__ void __launch_bounds__(NT, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [2]
-  uint64_t* q_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2], one arrival per softmax warp
-  uint64_t* p_full = bars + 9;   // one arrival per softmax warp
-  uint64_t* pd_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint64_t* info_full = bars + 12;  // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 14;  // [2], one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* q_full = bars + 1;          // [QS]
+  uint64_t* q_empty = bars + 1 + QS;    // [QS]
+  uint64_t* s_full = bars + 1 + 2 * QS;    // [2]
+  uint64_t* s_free = bars + 3 + 2 * QS;    // [2], one arrival per softmax warp
+  uint64_t* p_full = bars + 5 + 2 * QS;    // one arrival per softmax warp
+  uint64_t* pd_done = bars + 6 + 2 * QS;
+  uint64_t* drain = bars + 7 + 2 * QS;
+  uint64_t* info_full = bars + 8 + 2 * QS;   // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 10 + 2 * QS;  // [2], one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12 + 2 * QS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][64]
   float* info_dl = info_lse + 2 * 64;                                 // [2][64]
@@ -650,9 +660,11 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < QS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], NSW);
     }
@@ -695,7 +707,8 @@ __global__ void __launch_bounds__(NT, 1)
   }
 
   if (warp == 0 && lane == 0) {
-    int armed[3] = {-1, -1, -1};
+    int armed[1 + QS];
+    for (int i = 0; i < 1 + QS; ++i) armed[i] = -1;
     mbar_arrive_expect_tx(kv_full, 4 * KATOM);
     tma_load_3d(smem + K_OFF, &tmK, kv_full, 0, j0, b);
     tma_load_3d(smem + K_OFF + KATOM, &tmK, kv_full, 64, j0, b);
@@ -703,22 +716,24 @@ __global__ void __launch_bounds__(NT, 1)
     tma_load_3d(smem + V_OFF + KATOM, &tmV, kv_full, 64, j0, b);
     armed[0] = 0;
     for (int i = 0; i < n_rt; ++i) {
-      const int st = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
+      const int qs = i % QS;
+      const uint32_t qph = (i / QS) & 1;
       const int rr = (int)((rt0 + i) * BQ);
-      if (!sync.wait(&q_empty[st], ph ^ 1u)) break;
-      mbar_arrive_expect_tx(&q_full[st], 4 * QATOM);
-      tma_load_3d(smem + Q_OFF + st * 16384, &tmQ, &q_full[st], 0, rr, b);
-      tma_load_3d(smem + Q_OFF + st * 16384 + QATOM, &tmQ, &q_full[st], 64, rr, b);
-      tma_load_3d(smem + DO_OFF + st * 16384, &tmDO, &q_full[st], 0, rr, b);
-      tma_load_3d(smem + DO_OFF + st * 16384 + QATOM, &tmDO, &q_full[st], 64, rr, b);
-      armed[1 + st] = (int)ph;
+      if (!sync.wait(&q_empty[qs], qph ^ 1u)) break;
+      mbar_arrive_expect_tx(&q_full[qs], 4 * QATOM);
+      tma_load_3d(smem + Q_OFF + qs * 16384, &tmQ, &q_full[qs], 0, rr, b);
+      tma_load_3d(smem + Q_OFF + qs * 16384 + QATOM, &tmQ, &q_full[qs], 64, rr, b);
+      tma_load_3d(smem + DO_OFF + qs * 16384, &tmDO, &q_full[qs], 0, rr, b);
+      tma_load_3d(smem + DO_OFF + qs * 16384 + QATOM, &tmDO, &q_full[qs], 64, rr, b);
+      armed[1 + qs] = (int)qph;
     }
     if (*abort_flag) {
       int none = 0;
-      uint64_t* fb[3] = {kv_full, &q_full[0], &q_full[1]};
-      for (int i = 0; i < 3; ++i)
-        if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
+      if (armed[0] >= 0) mbar_wait_bounded(kv_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      for (int i = 0; i < QS; ++i)
+        if (armed[1 + i] >= 0)
+          mbar_wait_bounded(&q_full[i], (uint32_t)armed[1 + i], &none, err, SITE_ATTN,
+                            timeout_ns / 8);
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
@@ -727,12 +742,13 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t sPt = smem_u32(smem + PT_OFF), sdSt = smem_u32(smem + DST_OFF);
     bool ok = sync.wait(kv_full, 0), issued = false;
     auto issue_s = [&](int i) -> bool {
-      const int st = i & 1;
+      const int st = i & 1;  // TMEM S^T / dP^T buffer
       const uint32_t ph = (i >> 1) & 1;
-      if (!sync.wait(&q_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+      const int qs = i % QS;  // shared-memory Q / dO stage
+      if (!sync.wait(&q_full[qs], (i / QS) & 1) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
       tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + st * 16384);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + st * 16384);
+      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
         umma_bf16(tmem + st * 64, desc_k_atoms(sK, kk, KATOM), desc_k_atoms(sQ, kk, QATOM), idS,
@@ -748,11 +764,11 @@ __global__ void __launch_bounds__(NT, 1)
     if (ok) ok = issue_s(0);
     for (int i = 0; ok && i < n_rt; ++i) {
       if (i + 1 < n_rt && !issue_s(i + 1)) { ok = false; break; }
-      const int st = i & 1;
+      const int qs = i % QS;
       if (!sync.wait(p_full, i & 1)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + st * 16384);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + st * 16384);
+      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk)
         umma_bf16(tmem + 256, desc_k_atoms(sPt, kk, KATOM), desc_mn_blocks(sDO, kk, QATOM), idG,
@@ -762,7 +778,7 @@ __global__ void __launch_bounds__(NT, 1)
         umma_bf16(tmem + 384, desc_k_atoms(sdSt, kk, KATOM), desc_mn_blocks(sQ, kk, QATOM), idG,
                   (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit(pd_done);
-      umma_commit(&q_empty[st]);
+      umma_commit(&q_empty[qs]);
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;

@@ -23,9 +23,9 @@ inline cudaError_t launched(int n) {
 }
 
 // Query rows (tokens x heads) of one sequence that the attention kernels
-// accept: their tiles are indexed by the grid's y dimension (<= 65535 tiles
-// of 128 rows).
-constexpr long kMaxAttnRowsPerSeq = 65535L * 128;
+// accept: their 128-row tiles are indexed by the grid's y dimension (at most
+// 65535, and the forward launches whole CTA pairs).
+constexpr long kMaxAttnRowsPerSeq = 65534L * 128;
 
 enum GemmLayout { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_ADD_F32 = 2, EPI_RELU2 = 3,

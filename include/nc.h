@@ -159,6 +159,45 @@ nc_status nc_get_device_status(void* ws, void* stream);
 const char* nc_status_string(nc_status s);
 const char* nc_last_error_message(void);
 
+/* ---- optimizer step ------------------------------------------------------
+ * The update that follows a step (architecture list: Muon + AdamW, after
+ * modded-nanoGPT; walkthrough, pretraining section: Muon for the matrices,
+ * AdamW for the embedding and the unembedding, learning rates scaled by
+ * 1/sqrt(dim), lrm falling linearly to 0 at the end of training).
+ *
+ * Every tensor here is a device pointer the caller owns.  Master weights,
+ * gradients and optimizer state are float32 (same shapes as the weights);
+ * each updated master is also written to its compute copy (the bf16 or
+ * float weights the step reads, per cfg->dtype).
+ *   AdamW (wte, w_lm): m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
+ *     w <- w - lr wd w - lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps),
+ *     lr = lr_embed (wte) or lr_lm (w_lm) times lrm / sqrt(d_model).
+ *   Muon (every block matrix, r x c): b <- mu b + g; u = g + mu b;
+ *     X = u / (||u||_F + 1e-7) (transposed when r > c), then ns_steps of
+ *     X <- a X + (b A + c A A) X with A = X X^T (act-type batched GEMMs, all
+ *     layers of one shape at once); w <- w - lr_muon lrm sqrt(max(1, r/c)) X.
+ * t counts optimizer steps from 1 (AdamW bias correction).  lrm is the
+ * caller's schedule value for this step.  ws: >= nc_optimizer_workspace_bytes
+ * (scratch for the Newton-Schulz iterates, and the error word).  The result
+ * is a deterministic function of the inputs (fixed-order reductions). */
+typedef struct {
+  float lr_muon, momentum;                  /* Muon */
+  float lr_embed, lr_lm;                    /* AdamW rates before lrm / sqrt(d_model) */
+  float beta1, beta2, eps, weight_decay;    /* AdamW */
+  float ns_a, ns_b, ns_c;                   /* Newton-Schulz odd polynomial */
+  int ns_steps;
+} nc_opt_config;
+typedef struct { float *w_qkv, *w_o, *w_fc, *w_proj; } nc_layer_f;   /* float32 per-layer */
+typedef struct { void *w_qkv, *w_o, *w_fc, *w_proj; } nc_layer_wc;   /* compute copies */
+size_t nc_optimizer_workspace_bytes(const nc_config* cfg);
+nc_status nc_optimizer_step(const nc_config* cfg, const nc_opt_config* oc, int t, float lrm,
+                            float* wte, float* w_lm, const nc_layer_f* layers,
+                            void* wte_c, void* w_lm_c, const nc_layer_wc* layers_c,
+                            const float* dwte, const float* dw_lm, const nc_layer_g* grads,
+                            float* m_wte, float* v_wte, float* m_lm, float* v_lm,
+                            const nc_layer_f* momentum_bufs, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* ---- building blocks (the same kernels the step uses), for tests -------- */
 
 /* Bias-free linear layer contraction on the step's GEMM kernels
@@ -187,6 +226,19 @@ nc_status nc_gemm(int dtype, int layout, int epilogue, int M, int N, int K,
                   const void* A, int lda, const void* Bm, int ldb, void* C, int ldc,
                   const void* aux, int accumulate, void* ws, size_t ws_bytes,
                   void* stream);
+
+/* Batched contraction on the same kernels: `batch` independent products
+ * C_z = op(A_z, B_z), z = 0..batch-1, with A_z = A + z a_bstride,
+ * B_z = Bm + z b_bstride, C_z = C + z c_bstride (element strides, multiples
+ * of 8).  epilogue NC_EPI_STORE (C act type = acc) or NC_EPI_AXPBY (C act type
+ * = alpha aux_z + beta acc, aux_z = aux + z c_bstride, same layout as C).
+ * The Muon update's Newton-Schulz steps are built from it.  Same shape rules
+ * as nc_gemm; batch >= 1; no workspace beyond the error word (ws >= 256 B). */
+enum { NC_EPI_AXPBY = 6 };
+nc_status nc_gemm_batched(int dtype, int layout, int epilogue, int batch, int M, int N, int K,
+                          const void* A, int lda, long a_bstride, const void* Bm, int ldb,
+                          long b_bstride, void* C, int ldc, long c_bstride, const void* aux,
+                          float alpha, float beta, void* ws, size_t ws_bytes, void* stream);
 
 /* Causal multi-query attention alone (architecture list: MQA; causal from the
  * next-token objective).  q (B, T, H, h), k and v (B, T, h), o (B, T, H, h),

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libnc.so")
 SOURCES = ["nc_api.cu", "gemm.cu", "norm_rope.cu", "attention.cu", "attention_tc.cu", "loss.cu",
-           "embed_bwd.cu"]
+           "embed_bwd.cu", "optimizer.cu"]
 HEADERS = ["nc_common.cuh", "nc_internal.h", "epilogue.cuh", "gemm_tc.cuh", "tc_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -1,10 +1,16 @@
 // GEMM epilogues shared by the tcgen05 kernel (bf16) and the SIMT kernel (fp32).
 //
 // Each epilogue receives W consecutive fp32 accumulators of one output row,
-// starting at column `col` (W = 32 in the tensor-core kernel, W = 4 in the
-// SIMT kernel), and returns a per-chunk contribution to a row reduction that
-// only the softcap/cross-entropy epilogue uses.  The caller guarantees
-// row < M and col + W <= N.
+// starting at column `col`, and returns a per-chunk contribution to a row
+// reduction that only the softcap/cross-entropy epilogue uses.  The caller
+// guarantees row < M and col + W <= N.
+//
+//   apply<W>    (SIMT kernel, W = 4): transform and store to global memory.
+//   compute<W>  (tensor-core kernel, W = 128 bytes of Out): transform in
+//               registers only; the kernel stages the chunk in shared memory
+//               and writes it with one TMA bulk store, or a TMA bulk
+//               reduce-add into the destination when reduce() is true.
+//   Out         element type of the destination.
 #pragma once
 
 #include "nc_common.cuh"
@@ -33,8 +39,12 @@ __device__ __forceinline__ void load_row_chunk(const T* p, float (&v)[W]) {
 template <typename TOut>
 struct EpiStore {
   static constexpr bool kRowReduce = false;
+  using Out = TOut;
   TOut* c;
   long ldc;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  template <int W>
+  __device__ __forceinline__ float compute(int, int, float (&)[W], int) const { return 0.f; }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
     store_row_chunk<TOut, W>(c + (long)row * ldc + col, v);
@@ -48,10 +58,14 @@ struct EpiStore {
 // fixed order; with one split the epilogue writes (or accumulates into) C.
 struct EpiStoreF32 {
   static constexpr bool kRowReduce = false;
+  using Out = float;
   float* c;
   long ldc;
   long split_stride;
   int accumulate;
+  __device__ __forceinline__ bool reduce() const { return accumulate != 0; }
+  template <int W>
+  __device__ __forceinline__ float compute(int, int, float (&)[W], int) const { return 0.f; }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int split) const {
     float* p = c + split * split_stride + (long)row * ldc + col;
@@ -70,8 +84,12 @@ struct EpiStoreF32 {
 // Residual add into the float32 stream: X += acc.
 struct EpiAddF32 {
   static constexpr bool kRowReduce = false;
+  using Out = float;
   float* x;
   long ldx;
+  __device__ __forceinline__ bool reduce() const { return true; }
+  template <int W>
+  __device__ __forceinline__ float compute(int, int, float (&)[W], int) const { return 0.f; }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
     float* p = x + (long)row * ldx + col;
@@ -90,8 +108,19 @@ struct EpiAddF32 {
 template <typename TOut>
 struct EpiRelu2 {
   static constexpr bool kRowReduce = false;
+  using Out = TOut;
   TOut* a;
   long lda;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  template <int W>
+  __device__ __forceinline__ float compute(int, int, float (&v)[W], int) const {
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const float r = fmaxf(v[i], 0.f);
+      v[i] = r * r;
+    }
+    return 0.f;
+  }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
 #pragma unroll
@@ -110,31 +139,33 @@ struct EpiRelu2 {
 template <typename TOut>
 struct EpiRelu2Bwd {
   static constexpr bool kRowReduce = false;
+  using Out = TOut;
   // The tensor-core epilogue loads this tile row's `a` slice before it waits
   // for the accumulator, so the global-load latency overlaps the main loop.
   static constexpr bool kPrefetch = true;
+  static constexpr int kPreCols = 128 / sizeof(TOut);  // one 128-byte chunk of a
   struct Pre {
-    uint4 q[32 * sizeof(TOut) / 16];  // 32 elements of a
+    uint4 q[8];
   };
   TOut* du;
   const TOut* a;
   long ld;
+  __device__ __forceinline__ bool reduce() const { return false; }
   __device__ __forceinline__ static float two_sqrt(float x) {
     float r;
     asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
     return 2.f * r;
   }
-  __device__ __forceinline__ void prefetch(int row, int col, Pre& p) const {
+  __device__ __forceinline__ void prefetch(int row, int col, int, Pre& p) const {
     const uint4* src = reinterpret_cast<const uint4*>(a + (long)row * ld + col);
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(Pre) / 16); ++i) p.q[i] = __ldg(src + i);
+    for (int i = 0; i < 8; ++i) p.q[i] = __ldg(src + i);
   }
-  __device__ __forceinline__ float apply_pre(int row, int col, float (&v)[32], int,
-                                             const Pre& p) const {
+  __device__ __forceinline__ float compute_pre(int, int, float (&v)[kPreCols], int,
+                                               const Pre& p) const {
     const TOut* av = reinterpret_cast<const TOut*>(p.q);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= two_sqrt(to_f(av[i]));
-    store_row_chunk<TOut, 32>(du + (long)row * ld + col, v);
+    for (int i = 0; i < kPreCols; ++i) v[i] *= two_sqrt(to_f(av[i]));
     return 0.f;
   }
   template <int W>
@@ -149,6 +180,49 @@ struct EpiRelu2Bwd {
   __device__ __forceinline__ void row_end(int, int, float) const {}
 };
 
+// C = alpha * aux + beta * acc (aux of the output type, same layout as C;
+// batch entry z reads aux + z * aux_bstride).  The Newton-Schulz steps of
+// the Muon update use it: B = b A + c A A and X' = a X + B X.
+template <typename TOut>
+struct EpiAxpby {
+  static constexpr bool kRowReduce = false;
+  using Out = TOut;
+  static constexpr bool kPrefetch = true;
+  static constexpr int kPreCols = 128 / sizeof(TOut);
+  struct Pre {
+    uint4 q[8];
+  };
+  TOut* c;
+  const TOut* aux;
+  long ld;
+  long aux_bstride;
+  float alpha, beta;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  __device__ __forceinline__ void prefetch(int row, int col, int z, Pre& p) const {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(aux + (long)z * aux_bstride + (long)row * ld + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p.q[i] = __ldg(src + i);
+  }
+  __device__ __forceinline__ float compute_pre(int, int, float (&v)[kPreCols], int,
+                                               const Pre& p) const {
+    const TOut* av = reinterpret_cast<const TOut*>(p.q);
+#pragma unroll
+    for (int i = 0; i < kPreCols; ++i) v[i] = alpha * to_f(av[i]) + beta * v[i];
+    return 0.f;
+  }
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int z) const {
+    float av[W];
+    load_row_chunk<TOut, W>(aux + (long)z * aux_bstride + (long)row * ld + col, av);
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = alpha * av[i] + beta * v[i];
+    store_row_chunk<TOut, W>(c + (long)z * aux_bstride + (long)row * ld + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
 // LM head epilogue (tensor-core path): s = c tanh(z / c) stored as fp16 --
 // |s| <= c = 15 lies well inside fp16's range and fp16 keeps 3 more mantissa
 // bits than bf16 there; the per-row sum of exp(s) over this tile's columns
@@ -157,6 +231,7 @@ struct EpiRelu2Bwd {
 // is kept in fp32 (s_tgt) for the loss.
 struct EpiSoftcapCE {
   static constexpr bool kRowReduce = true;
+  using Out = __half;
   __half* s;
   long lds;
   float* part;
@@ -165,6 +240,21 @@ struct EpiSoftcapCE {
   const int* targets;
   float* s_tgt;
   float cap, inv_cap;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  template <int W>
+  __device__ __forceinline__ float compute(int row, int col, float (&v)[W], int) const {
+    const int y = __ldg(targets + row);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      float t;
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(v[i] * inv_cap));
+      v[i] = cap * t;
+      sum += __expf(v[i]);
+      if (col + i == y) s_tgt[row] = v[i];
+    }
+    return sum;
+  }
   template <int W>
   __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
     const int y = __ldg(targets + row);

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "epilogue.cuh"
@@ -90,7 +91,7 @@ static cudaError_t dispatch_f32(const GemmArgs& g, const Epi& epi, const Ctx& ct
   return cudaErrorInvalidValue;
 }
 
-cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx) {
+cudaError_t gemm_f32_one(const GemmArgs& g, const Ctx& ctx) {
   switch (g.epi) {
     case EPI_STORE: return dispatch_f32(g, EpiStore<float>{static_cast<float*>(g.C), g.ldc}, ctx);
     case EPI_STORE_F32:
@@ -102,8 +103,29 @@ cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx) {
                           EpiRelu2Bwd<float>{static_cast<float*>(g.C),
                                              static_cast<const float*>(g.aux), g.ldc},
                           ctx);
+    case EPI_AXPBY:
+      return dispatch_f32(g,
+                          EpiAxpby<float>{static_cast<float*>(g.C),
+                                          static_cast<const float*>(g.aux), g.ldc, 0, g.alpha,
+                                          g.beta},
+                          ctx);
   }
   return cudaErrorInvalidValue;
+}
+
+// The fp32 SIMT path runs a batched product as one launch per entry.
+cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx) {
+  const int nb = g.batch > 1 ? g.batch : 1;
+  for (int z = 0; z < nb; ++z) {
+    GemmArgs e = g;
+    e.A = static_cast<const float*>(g.A) + z * g.a_bstride;
+    e.B = static_cast<const float*>(g.B) + z * g.b_bstride;
+    e.C = static_cast<float*>(g.C) + z * g.c_bstride;
+    if (g.aux) e.aux = static_cast<const float*>(g.aux) + z * g.c_bstride;
+    cudaError_t r = gemm_f32_one(e, ctx);
+    if (r != cudaSuccess) return r;
+  }
+  return cudaSuccess;
 }
 
 // ===================================================================
@@ -119,16 +141,17 @@ struct Plan {
   tc::Sched sch;
 };
 
-Plan make_plan(int layout, int epi, int M, int N, int K, int group_m) {
+Plan make_plan(int layout, int epi, int M, int N, int K, int group_m, int batch = 1) {
   Plan p;
   tc::Sched& s = p.sch;
+  s.batches = batch > 1 ? batch : 1;
   s.m_tiles = (M + tc::BM - 1) / tc::BM;
   s.n_tiles = (N + tc::BN - 1) / tc::BN;
   s.k_blocks = (K + tc::BK - 1) / tc::BK;
   s.splits = 1;
   s.kb_per_split = s.k_blocks;
   const int tiles = s.m_tiles * s.n_tiles;
-  if (epi == EPI_STORE_F32 && tiles < 2 * kSplitUnits && s.k_blocks >= 32) {
+  if (epi == EPI_STORE_F32 && s.batches == 1 && tiles < 2 * kSplitUnits && s.k_blocks >= 32) {
     // Split the reduction so that the units fill the SMs; cost proxy =
     // waves x k-blocks per unit, plus one k-block per split for the slab pass.
     long best = -1;
@@ -147,7 +170,7 @@ Plan make_plan(int layout, int epi, int M, int N, int K, int group_m) {
     }
   }
   s.group_m = group_m > 0 ? group_m : 8;
-  s.units = tiles * s.splits;
+  s.units = tiles * s.splits * s.batches;
   (void)layout;
   return p;
 }
@@ -166,29 +189,59 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major (outer x inner) matrix with row stride
-// `ld` elements; 128-byte swizzle; out-of-range elements read as zero.
+// bf16 tensor map over `nb` row-major (outer x inner) matrices with row
+// stride `ld` and matrix stride `bstride` elements (dims {inner, outer, nb});
+// 128-byte swizzle; out-of-range elements read as zero.
 bool make_tmap(CUtensorMap* m, const void* base, long inner, long outer, long ld, int box_inner,
-               int box_outer) {
+               int box_outer, long nb = 1, long bstride = 0) {
   auto enc = tmap_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  if (nb < 1) nb = 1;
+  if (bstride <= 0) bstride = outer * ld;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// Destination map for the epilogue's bulk stores: dims {N, M, Z} (Z split-K
+// slabs or batch entries, else 1), row stride `ld` elements, slab stride
+// `zstride` elements (0: M * ld), box {128 bytes, 128 rows, 1}.
+template <typename Out>
+bool make_tmap_out(CUtensorMap* m, void* base, long N, long M, long ld, long Z,
+                   long zstride = 0) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      sizeof(Out) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                       : (std::is_same<Out, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  const long es = sizeof(Out);
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)Z};
+  if (zstride <= 0) zstride = M * ld;
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(zstride * es)};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)tc::HALF_ROWS, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool A_MN, bool B_MN, class Epi>
-cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ctx& ctx) {
-  CUtensorMap ta, tb;
-  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
-                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, tc::HALF_ROWS);
-  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
-                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::HALF_ROWS));
+cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* out, long ldo,
+                      long zslabs, const Ctx& ctx) {
+  CUtensorMap ta, tb, tcm;
+  const long nb = p.sch.batches;
+  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64, nb, g.a_bstride)
+                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, tc::HALF_ROWS, nb, g.a_bstride);
+  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64, nb, g.b_bstride)
+                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::HALF_ROWS, nb, g.b_bstride));
+  ok = ok && make_tmap_out<typename Epi::Out>(&tcm, out, g.N, g.M, ldo, zslabs * nb,
+                                              nb > 1 ? g.c_bstride : 0);
   if (!ok) return cudaErrorInvalidValue;
   auto kern = tc::gemm_bf16_tc_kernel<A_MN, B_MN, Epi>;
   static bool attr_set = false;  // per instantiation
@@ -200,17 +253,18 @@ cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ct
   }
   // One CTA pair (a 2-CTA cluster) per unit, at most one CTA per SM.
   const int grid = 2 * std::max(1, std::min(p.sch.units, ctx.num_sms / 2));
-  kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, ctx.stream>>>(ta, tb, p.sch, g.M, g.N, epi, ctx.err,
-                                                             ctx.timeout_ns);
+  kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, ctx.stream>>>(ta, tb, tcm, p.sch, g.M, g.N, epi,
+                                                             ctx.err, ctx.timeout_ns);
   return launched(1);
 }
 
 template <class Epi>
-cudaError_t dispatch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, const Ctx& ctx) {
+cudaError_t dispatch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* out, long ldo,
+                        long zslabs, const Ctx& ctx) {
   switch (g.layout) {
-    case GEMM_NT: return launch_tc<false, false>(g, p, epi, ctx);
-    case GEMM_NN: return launch_tc<false, true>(g, p, epi, ctx);
-    case GEMM_TN: return launch_tc<true, true>(g, p, epi, ctx);
+    case GEMM_NT: return launch_tc<false, false>(g, p, epi, out, ldo, zslabs, ctx);
+    case GEMM_NN: return launch_tc<false, true>(g, p, epi, out, ldo, zslabs, ctx);
+    case GEMM_TN: return launch_tc<true, true>(g, p, epi, out, ldo, zslabs, ctx);
   }
   return cudaErrorInvalidValue;
 }
@@ -264,30 +318,41 @@ size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K) {
 }
 
 cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx) {
-  const Plan p = make_plan(g.layout, g.epi, g.M, g.N, g.K, g.group_m);
+  const Plan p = make_plan(g.layout, g.epi, g.M, g.N, g.K, g.group_m, g.batch);
   const bf16* aux = static_cast<const bf16*>(g.aux);
   switch (g.epi) {
-    case EPI_STORE: return dispatch_tc(g, p, EpiStore<bf16>{static_cast<bf16*>(g.C), g.ldc}, ctx);
+    case EPI_STORE:
+      return dispatch_tc(g, p, EpiStore<bf16>{static_cast<bf16*>(g.C), g.ldc}, g.C, g.ldc, 1,
+                         ctx);
     case EPI_STORE_F32: {
       if (p.sch.splits == 1)
         return dispatch_tc(g, p, EpiStoreF32{static_cast<float*>(g.C), g.ldc, 0, g.accumulate},
-                           ctx);
+                           g.C, g.ldc, 1, ctx);
       const size_t need = (size_t)p.sch.splits * g.M * g.N;
       if (!g.split_buf || g.split_buf_elems < need || g.ldc != g.N) return cudaErrorInvalidValue;
-      cudaError_t e = dispatch_tc(
-          g, p, EpiStoreF32{g.split_buf, (long)g.N, (long)g.M * g.N, 0}, ctx);
+      cudaError_t e = dispatch_tc(g, p, EpiStoreF32{g.split_buf, (long)g.N, (long)g.M * g.N, 0},
+                                  g.split_buf, g.N, p.sch.splits, ctx);
       if (e != cudaSuccess) return e;
       return splitk_reduce(static_cast<float*>(g.C), g.split_buf, p.sch.splits, (long)g.M * g.N,
                            g.accumulate, ctx);
     }
-    case EPI_ADD_F32: return dispatch_tc(g, p, EpiAddF32{static_cast<float*>(g.C), g.ldc}, ctx);
-    case EPI_RELU2: return dispatch_tc(g, p, EpiRelu2<bf16>{static_cast<bf16*>(g.C), g.ldc}, ctx);
+    case EPI_ADD_F32:
+      return dispatch_tc(g, p, EpiAddF32{static_cast<float*>(g.C), g.ldc}, g.C, g.ldc, 1, ctx);
+    case EPI_RELU2:
+      return dispatch_tc(g, p, EpiRelu2<bf16>{static_cast<bf16*>(g.C), g.ldc}, g.C, g.ldc, 1,
+                         ctx);
     case EPI_RELU2_BWD:
-      return dispatch_tc(g, p, EpiRelu2Bwd<bf16>{static_cast<bf16*>(g.C), aux, g.ldc}, ctx);
+      return dispatch_tc(g, p, EpiRelu2Bwd<bf16>{static_cast<bf16*>(g.C), aux, g.ldc}, g.C,
+                         g.ldc, 1, ctx);
     case EPI_SOFTCAP_CE: {
       EpiSoftcapCE e{static_cast<__half*>(g.C), g.ldc, g.part, g.n_part, tc::BN, g.targets,
                      g.s_tgt, g.cap, 1.f / g.cap};
-      return dispatch_tc(g, p, e, ctx);
+      return dispatch_tc(g, p, e, g.C, g.ldc, 1, ctx);
+    }
+    case EPI_AXPBY: {
+      EpiAxpby<bf16> e{static_cast<bf16*>(g.C), aux, g.ldc, g.batch > 1 ? g.c_bstride : 0,
+                       g.alpha, g.beta};
+      return dispatch_tc(g, p, e, g.C, g.ldc, 1, ctx);
     }
   }
   return cudaErrorInvalidValue;

@@ -19,7 +19,12 @@
 // Warp roles (256 threads per CTA): warp 0 lane 0 issues TMA (both CTAs;
 // completion is counted on the even CTA's barrier), warp 1 lane 0 of the
 // even CTA issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..7
-// run the epilogue (warp 4 + i reads TMEM lanes 32i..32i+31).  Every wait is
+// run the epilogue (warp 4 + i reads TMEM lanes 32i..32i+31, i.e. tile rows).
+// The epilogue transforms one 128-byte-wide column chunk of its 128 rows at a
+// time in registers, writes it to a 128B-swizzled staging buffer and lets one
+// thread store the chunk with a TMA bulk store (or bulk reduce-add for the
+// float32 residual / gradient accumulation), so global writes go out as
+// whole lines; two staging buffers alternate.  Every wait is
 // bounded: on timeout the CTA records DEV_TIMEOUT, its roles stop, in-flight
 // work is drained (bounded) and TMEM is released before the pair exits.
 #pragma once
@@ -45,18 +50,30 @@ constexpr int B_BYTES = HALF_ROWS * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 256;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+// Epilogue staging: two 128-row x 128-byte chunks of the output tile.
+constexpr int STAGE_OUT_BYTES = HALF_ROWS * 128;  // 16 KB
+constexpr int OUT_OFF = STAGES * STAGE_BYTES;
+constexpr int BAR_OFF = OUT_OFF + 2 * STAGE_OUT_BYTES;
+constexpr int SMEM_BYTES = BAR_OFF + 256 /*barriers*/ + 1024 /*align slack*/;
+static_assert(SMEM_BYTES <= 232448, "GEMM shared memory exceeds 227 KB");
 // Swizzle-128B atom: 8 rows of 128 bytes.  An MN-major operand half-tile is
 // stored as 128/64 = 2 column blocks of 64 elements, each BK rows of 128 B.
 constexpr int MN_BLOCK_BYTES = BK * 128;  // 8 KB
 
+// Work units, batch outermost (the tiles of one batch entry run together and
+// share its operands in L2), then k-split, then grouped (m, n) tiles.
 struct Sched {
-  int m_tiles, n_tiles, splits, k_blocks, kb_per_split, group_m, units;
+  int m_tiles, n_tiles, splits, k_blocks, kb_per_split, group_m, units, batches;
 
-  __device__ __forceinline__ void decode(int u, int& mt, int& nt, int& split, int& kb0,
+  // z: destination slab (batch * splits + split); batch: operand slice.
+  __device__ __forceinline__ void decode(int u, int& mt, int& nt, int& z, int& batch, int& kb0,
                                          int& kb1) const {
     const int per_split = m_tiles * n_tiles;
-    split = u / per_split;
+    const int per_batch = per_split * splits;
+    batch = u / per_batch;
+    u -= batch * per_batch;
+    const int split = u / per_split;
+    z = batch * splits + split;
     const int r = u - split * per_split;
     const int group_size = group_m * n_tiles;
     const int group = r / group_size;
@@ -114,23 +131,56 @@ enum WaitSite : int {
   SITE_EPI_ACC_FULL = 104, SITE_DRAIN = 105
 };
 
+// 128 bytes of one output row (W elements of Out) into row `r` of a
+// [128 rows][128 B] staging chunk with the TMA 128-byte swizzle.
+template <typename Out, int W>
+__device__ __forceinline__ void stage_row(uint8_t* chunk, int r, const float (&v)[W]) {
+  uint8_t* base = chunk + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 w;
+    if constexpr (sizeof(Out) == 4) {
+      w.x = __float_as_uint(v[q * 4 + 0]);
+      w.y = __float_as_uint(v[q * 4 + 1]);
+      w.z = __float_as_uint(v[q * 4 + 2]);
+      w.w = __float_as_uint(v[q * 4 + 3]);
+    } else {
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (std::is_same<Out, __half>::value) {
+          const __half2 t = __floats2half2_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+          h[e] = *reinterpret_cast<const uint32_t*>(&t);
+        } else {
+          const __nv_bfloat162 t = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+          h[e] = *reinterpret_cast<const uint32_t*>(&t);
+        }
+      }
+      w = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    *reinterpret_cast<uint4*>(base + ((q ^ (r & 7)) << 4)) = w;
+  }
+}
+
 template <bool A_MN, bool B_MN, class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const Sched sch, const int M,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const Sched sch, const int M,
                         const int N, const Epi epi, int* err, const long long timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_ok = abort_flag + 1;  // [4]: the epilogue warps' accumulator waits
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -154,6 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -174,8 +225,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) armed_phase[s] = -1;
     bool ok = true;
     for (int u = pair; u < sch.units && ok; u += npairs) {
-      int mt, nt, split, kb0, kb1;
-      sch.decode(u, mt, nt, split, kb0, kb1);
+      int mt, nt, split, batch, kb0, kb1;
+      sch.decode(u, mt, nt, split, batch, kb0, kb1);
       const int row_a = mt * BM + (int)rank * HALF_ROWS;
       const int row_b = nt * BN + (int)rank * HALF_ROWS;
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -193,18 +244,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         uint8_t* b = sB + stage * B_BYTES;
         const int k0 = kb * BK;
         if (!A_MN) {
-          tma_load_2d_pair(a, &tmA, bar, k0, row_a);
+          tma_load_3d_pair(a, &tmA, bar, k0, row_a, batch);
         } else {
 #pragma unroll
           for (int j = 0; j < HALF_ROWS / 64; ++j)
-            tma_load_2d_pair(a + j * MN_BLOCK_BYTES, &tmA, bar, row_a + 64 * j, k0);
+            tma_load_3d_pair(a + j * MN_BLOCK_BYTES, &tmA, bar, row_a + 64 * j, k0, batch);
         }
         if (!B_MN) {
-          tma_load_2d_pair(b, &tmB, bar, k0, row_b);
+          tma_load_3d_pair(b, &tmB, bar, k0, row_b, batch);
         } else {
 #pragma unroll
           for (int j = 0; j < HALF_ROWS / 64; ++j)
-            tma_load_2d_pair(b + j * MN_BLOCK_BYTES, &tmB, bar, row_b + 64 * j, k0);
+            tma_load_3d_pair(b + j * MN_BLOCK_BYTES, &tmB, bar, row_b + 64 * j, k0, batch);
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -231,8 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true, issued = false;
     for (int u = pair; u < sch.units && ok; u += npairs) {
-      int mt, nt, split, kb0, kb1;
-      sch.decode(u, mt, nt, split, kb0, kb1);
+      int mt, nt, split, batch, kb0, kb1;
+      sch.decode(u, mt, nt, split, batch, kb0, kb1);
       if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_flag, err,
                              SITE_MMA_ACC_EMPTY, timeout_ns)) {
         ok = false;
@@ -277,50 +328,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, 128 rows each) ----------------
+    using Out = typename Epi::Out;
+    constexpr int W = 128 / (int)sizeof(Out);  // columns per staging chunk
+    constexpr int NCH = BN / W;
     const int quarter = warp & 3;
+    const bool issuer = warp == 4 && lane == 0;
     const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&acc_empty[1]), 0);
-    int acc = 0;
+    const bool reduce = epi.reduce();
+    int acc = 0, chunk_no = 0;
     uint32_t acc_phase = 0;
     for (int u = pair; u < sch.units; u += npairs) {
-      int mt, nt, split, kb0, kb1;
-      sch.decode(u, mt, nt, split, kb0, kb1);
-      const int row = mt * BM + (int)rank * HALF_ROWS + quarter * 32 + lane;
+      int mt, nt, split, batch, kb0, kb1;
+      sch.decode(u, mt, nt, split, batch, kb0, kb1);
+      const int r_in = quarter * 32 + lane;
+      const int row0 = mt * BM + (int)rank * HALF_ROWS;
+      const int row = row0 + r_in;
       constexpr bool kPre = HasPrefetch<Epi>::value;
       using Pre = typename std::conditional<kPre, typename PreOf<Epi, kPre>::type, NoPre>::type;
-      Pre pre[kPre ? BN / 32 : 1];
+      Pre pre[kPre ? NCH : 1];
       if constexpr (kPre) {
+        static_assert(!kPre || Epi::kPreCols == W, "prefetch chunk must match the staging chunk");
         if (row < M) {
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            if (nt * BN + c * 32 < N) epi.prefetch(row, nt * BN + c * 32, pre[c]);
+          for (int c = 0; c < NCH; ++c)
+            if (nt * BN + c * W < N) epi.prefetch(row, nt * BN + c * W, batch, pre[c]);
         }
       }
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_cluster(&acc_full[acc], acc_phase, abort_flag, err, SITE_EPI_ACC_FULL,
                                timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // The four warps leave together or not at all (they meet at named
+      // barriers below).
+      if (lane == 0) epi_ok[quarter] = ok;
+      named_bar_sync<128>();
+      ok = epi_ok[0] & epi_ok[1] & epi_ok[2] & epi_ok[3];
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       float row_acc = 0.f;
-      if constexpr (kPre) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld_32cols(taddr + c * 32, v);
-          const int col = nt * BN + c * 32;
-          if (row < M && col < N) row_acc += epi.apply_pre(row, col, v, split, pre[c]);
+      for (int c = 0; c < NCH; ++c) {
+        const int col = nt * BN + c * W;
+        // Chunks wholly outside C are skipped by all four warps alike; only
+        // stored chunks take a staging buffer, so the newest pending store
+        // always reads the other buffer.
+        if (col >= N || row0 >= M) continue;
+        float v[W];
+#pragma unroll
+        for (int h = 0; h < W / 32; ++h)
+          tmem_ld_32cols(taddr + c * W + h * 32, *reinterpret_cast<float(*)[32]>(v + h * 32));
+        if (row < M) {
+          if constexpr (kPre)
+            row_acc += epi.compute_pre(row, col, v, batch, pre[c]);
+          else
+            row_acc += epi.template compute<W>(row, col, v, batch);
         }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld_32cols(taddr + c * 32, v);
-          const int col = nt * BN + c * 32;
-          if (row < M && col < N) row_acc += epi.template apply<32>(row, col, v, split);
+        uint8_t* chunk = smem + OUT_OFF + (chunk_no & 1) * STAGE_OUT_BYTES;
+        ++chunk_no;
+        if (issuer) bulk_wait_group_read<1>();  // the store issued from this buffer is done reading
+        named_bar_sync<128>();
+        stage_row<Out, W>(chunk, r_in, v);
+        fence_proxy_async_smem();
+        named_bar_sync<128>();
+        if (issuer) {
+          if (reduce)
+            tma_reduce_add_3d(&tmC, chunk, col, row0, split);
+          else
+            tma_store_3d(&tmC, chunk, col, row0, split);
+          bulk_commit_group();
         }
       }
       if (Epi::kRowReduce && row < M) epi.row_end(row, nt * BN, row_acc);
@@ -332,6 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    if (issuer) bulk_wait_group_all();
   }
 
   tc_fence_before();

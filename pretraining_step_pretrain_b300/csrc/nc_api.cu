@@ -582,6 +582,104 @@ nc_status nc_gemm(int dtype, int layout, int epilogue, int M, int N, int K, cons
   return NC_OK;
 }
 
+nc_status nc_gemm_batched(int dtype, int layout, int epilogue, int batch, int M, int N, int K,
+                          const void* A, int lda, long a_bstride, const void* Bm, int ldb,
+                          long b_bstride, void* C, int ldc, long c_bstride, const void* aux,
+                          float alpha, float beta, void* ws, size_t ws_bytes, void* stream) {
+  if (dtype != NC_BF16 && dtype != NC_F32) return fail(NC_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  if (layout < NC_GEMM_NT || layout > NC_GEMM_TN)
+    return fail(NC_ERR_INVALID_ARG, "bad layout %d", layout);
+  if (epilogue != NC_EPI_STORE && epilogue != NC_EPI_AXPBY)
+    return fail(NC_ERR_INVALID_ARG, "batched epilogue %d is not STORE or AXPBY", epilogue);
+  if (batch < 1 || M < 1 || N < 1 || K < 1 || N % 32)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "batch=%d M=%d N=%d K=%d: need >= 1 and N %% 32 == 0",
+                batch, M, N, K);
+  if (lda % 8 || ldb % 8 || ldc % 8 || a_bstride % 8 || b_bstride % 8 || c_bstride % 8)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "leading dimensions and batch strides must be multiples of 8");
+  const long a_min = layout == NC_GEMM_TN ? M : K;
+  const long b_min = layout == NC_GEMM_NT ? K : N;
+  if (lda < a_min || ldb < b_min || ldc < N)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "leading dimension smaller than the row length");
+  const long a_rows = layout == NC_GEMM_TN ? K : M, b_rows = layout == NC_GEMM_NT ? N : K;
+  if (batch > 1 && (a_bstride < a_rows * lda || b_bstride < b_rows * ldb || c_bstride < (long)M * ldc))
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "batch entries overlap (stride smaller than a matrix)");
+  nc_status s = check_ptrs({A, Bm, C, ws});
+  if (s != NC_OK) return s;
+  if (epilogue == NC_EPI_AXPBY && ((s = check_ptrs({aux})) != NC_OK)) return s;
+  if (ws_bytes < 256) return fail(NC_ERR_WORKSPACE, "gemm workspace too small");
+  GemmArgs g = gemm_args(layout, epilogue, M, N, K, A, lda, Bm, ldb, C, ldc);
+  g.aux = aux;
+  g.batch = batch;
+  g.a_bstride = a_bstride;
+  g.b_bstride = b_bstride;
+  g.c_bstride = c_bstride;
+  g.alpha = alpha;
+  g.beta = beta;
+  const Ctx ctx = make_ctx(ws, stream);
+  cudaError_t e = dtype == NC_BF16 ? gemm_bf16(g, ctx) : gemm_f32(g, ctx);
+  if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  return NC_OK;
+}
+
+size_t nc_optimizer_workspace_bytes(const nc_config* cfg) {
+  if (!cfg || check_cfg(cfg, 1, 1) != NC_OK) return 0;
+  return optimizer_ws_bytes(*cfg);
+}
+
+nc_status nc_optimizer_step(const nc_config* cfg, const nc_opt_config* oc, int t, float lrm,
+                            float* wte, float* w_lm, const nc_layer_f* layers, void* wte_c,
+                            void* w_lm_c, const nc_layer_wc* layers_c, const float* dwte,
+                            const float* dw_lm, const nc_layer_g* grads, float* m_wte,
+                            float* v_wte, float* m_lm, float* v_lm,
+                            const nc_layer_f* momentum_bufs, void* ws, size_t ws_bytes,
+                            void* stream) {
+  nc_status s = check_cfg(cfg, 1, 1);
+  if (s != NC_OK) return s;
+  if (!oc || !layers || !layers_c || !grads || !momentum_bufs)
+    return fail(NC_ERR_INVALID_ARG, "null optimizer config or per-layer array");
+  if (t < 1) return fail(NC_ERR_INVALID_ARG, "optimizer step t=%d must be >= 1", t);
+  if (oc->ns_steps < 0 || oc->ns_steps > 64)
+    return fail(NC_ERR_INVALID_ARG, "ns_steps %d outside [0, 64]", oc->ns_steps);
+  if (!(oc->beta1 >= 0.f && oc->beta1 < 1.f) || !(oc->beta2 >= 0.f && oc->beta2 < 1.f) ||
+      !(oc->eps > 0.f))
+    return fail(NC_ERR_INVALID_ARG, "AdamW betas must lie in [0, 1) and eps > 0");
+  if ((s = check_ptrs({wte, w_lm, wte_c, w_lm_c, dwte, dw_lm, m_wte, v_wte, m_lm, v_lm, ws})) !=
+      NC_OK)
+    return s;
+  for (int l = 0; l < cfg->depth; ++l) {
+    const nc_layer_f& p = layers[l];
+    const nc_layer_wc& c = layers_c[l];
+    const nc_layer_g& g = grads[l];
+    const nc_layer_f& m = momentum_bufs[l];
+    if ((s = check_ptrs({p.w_qkv, p.w_o, p.w_fc, p.w_proj, c.w_qkv, c.w_o, c.w_fc, c.w_proj,
+                         g.d_qkv, g.d_o, g.d_fc, g.d_proj, m.w_qkv, m.w_o, m.w_fc, m.w_proj})) !=
+        NC_OK) {
+      const std::string why = nc_last_error_message();
+      return fail(s, "layer %d: %s", l, why.c_str());
+    }
+  }
+  if (ws_bytes < optimizer_ws_bytes(*cfg)) return fail(NC_ERR_WORKSPACE, "optimizer workspace too small");
+  OptTensors w;
+  w.wte = wte;
+  w.w_lm = w_lm;
+  w.layers = layers;
+  w.wte_c = wte_c;
+  w.w_lm_c = w_lm_c;
+  w.layers_c = layers_c;
+  w.dwte = dwte;
+  w.dw_lm = dw_lm;
+  w.grads = grads;
+  w.m_wte = m_wte;
+  w.v_wte = v_wte;
+  w.m_lm = m_lm;
+  w.v_lm = v_lm;
+  w.mom = momentum_bufs;
+  const Ctx ctx = make_ctx(ws, stream);
+  cudaError_t e = optimizer_step(*cfg, *oc, t, lrm, w, ws, ctx);
+  if (e != cudaSuccess) return fail(NC_ERR_CUDA, "optimizer launch: %s", cudaGetErrorString(e));
+  return NC_OK;
+}
+
 long long nc_launch_count(void) { return g_launches.load(); }
 
 nc_status nc_profile_start(int max_records) {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "nc.h"
+
 namespace nc {
 
 struct Ctx {
@@ -29,7 +31,7 @@ constexpr long kMaxAttnRowsPerSeq = 65534L * 128;
 
 enum GemmLayout { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_ADD_F32 = 2, EPI_RELU2 = 3,
-               EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5 };
+               EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5, EPI_AXPBY = 6 };
 
 struct GemmArgs {
   int layout, epi;
@@ -44,6 +46,12 @@ struct GemmArgs {
   // STORE_F32 split-K slabs (tensor-core path); may be null when not needed
   float* split_buf; size_t split_buf_elems;
   int group_m;            // m-tiles per raster group (0 = default)
+  // Batched GEMM: `batch` independent products (0 or 1 = one); entry z uses
+  // A + z a_bstride, B + z b_bstride, C + z c_bstride, aux + z c_bstride
+  // (element strides).  Not combined with split-K.
+  int batch;
+  long a_bstride, b_bstride, c_bstride;
+  float alpha, beta;      // AXPBY: C = alpha * aux + beta * acc
 };
 
 // bf16 tensor map with 128-byte swizzle and zero fill out of range.  dims[0]
@@ -120,4 +128,33 @@ cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const flo
 // Test hook: a CTA waiting on an mbarrier nothing completes (bounded).
 cudaError_t selftest_wait(long long timeout_ns, const Ctx& ctx);
 
+// ---- optimizer (optimizer.cu) ------------------------------------------
+struct AdamWArgs {
+  float lr, beta1, beta2, eps, wd, inv_bc1, inv_bc2;
+};
+cudaError_t adamw_step(bool bf16_copy, float* p, const float* g, float* m, float* v, void* pc,
+                       long n, const AdamWArgs& a, const Ctx& ctx);
+cudaError_t muon_momentum(const float* g, float* b, long n, float mu, float* partial,
+                          const Ctx& ctx);
+cudaError_t muon_prepare(bool bf16, const float* g, const float* b, float mu,
+                         const float* partial, int r, int c, bool transpose, void* x,
+                         const Ctx& ctx);
+cudaError_t muon_update(bool bf16, float* p, const void* x, int r, int c, bool transpose,
+                        float step, void* pc, const Ctx& ctx);
+int muon_partials();
+
+// Host side of the optimizer step (optimizer.cu), on the C-ABI types.
+struct OptTensors {
+  float *wte, *w_lm;
+  const nc_layer_f* layers;
+  void *wte_c, *w_lm_c;
+  const nc_layer_wc* layers_c;
+  const float *dwte, *dw_lm;
+  const nc_layer_g* grads;
+  float *m_wte, *v_wte, *m_lm, *v_lm;
+  const nc_layer_f* mom;
+};
+size_t optimizer_ws_bytes(const nc_config& c);
+cudaError_t optimizer_step(const nc_config& c, const nc_opt_config& oc, int t, float lrm,
+                           const OptTensors& w, void* ws, const Ctx& ctx);
 }  // namespace nc

@@ -17,6 +17,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnc.so")
 NC_BF16, NC_F32 = 0, 1
 GEMM_NT, GEMM_NN, GEMM_TN = 0, 1, 2
 EPI_STORE, EPI_STORE_F32, EPI_ADD_F32, EPI_RELU2, EPI_RELU2_BWD = 0, 1, 2, 3, 4
+EPI_AXPBY = 6
 STATUS = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED_SHAPE",
           3: "NC_ERR_WORKSPACE", 4: "NC_ERR_CUDA", 5: "NC_ERR_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
 
@@ -27,7 +28,8 @@ EXPORTS = ("nc_workspace_bytes", "nc_embed_norm", "nc_block_fwd", "nc_lmhead_sof
            "nc_attention_workspace_bytes", "nc_attention_fwd", "nc_attention_bwd",
            "nc_attention_bwd_noalloc",
            "nc_launch_count", "nc_profile_start", "nc_profile_stop", "nc_profile_record",
-           "nc_selftest_wait_timeout")
+           "nc_selftest_wait_timeout", "nc_gemm_batched", "nc_optimizer_workspace_bytes",
+           "nc_optimizer_step")
 
 
 class NcConfig(ctypes.Structure):
@@ -45,6 +47,26 @@ class NcLayerW(ctypes.Structure):
 class NcLayerG(ctypes.Structure):
     _fields_ = [("d_qkv", ctypes.c_void_p), ("d_o", ctypes.c_void_p),
                 ("d_fc", ctypes.c_void_p), ("d_proj", ctypes.c_void_p)]
+
+
+class NcLayerF(ctypes.Structure):
+    """float32 per-layer matrices (master weights or Muon momentum buffers)."""
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("w_fc", ctypes.c_void_p), ("w_proj", ctypes.c_void_p)]
+
+
+class NcLayerWC(ctypes.Structure):
+    """Per-layer compute copies the optimizer rewrites."""
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("w_fc", ctypes.c_void_p), ("w_proj", ctypes.c_void_p)]
+
+
+class NcOptConfig(ctypes.Structure):
+    _fields_ = [("lr_muon", ctypes.c_float), ("momentum", ctypes.c_float),
+                ("lr_embed", ctypes.c_float), ("lr_lm", ctypes.c_float),
+                ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("ns_a", ctypes.c_float),
+                ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float), ("ns_steps", ctypes.c_int)]
 
 
 class NcError(RuntimeError):
@@ -92,6 +114,14 @@ def lib() -> ctypes.CDLL:
             "nc_profile_stop": (I, []),
             "nc_profile_record": (I, [I, ctypes.POINTER(ctypes.c_char_p),
                                       ctypes.POINTER(ctypes.c_float)]),
+            "nc_gemm_batched": (I, [I, I, I, I, I, I, I, P, I, ctypes.c_long, P, I, ctypes.c_long,
+                                    P, I, ctypes.c_long, P, ctypes.c_float, ctypes.c_float, P, S,
+                                    P]),
+            "nc_optimizer_workspace_bytes": (S, [C]),
+            "nc_optimizer_step": (I, [C, ctypes.POINTER(NcOptConfig), I, ctypes.c_float, P, P,
+                                      ctypes.POINTER(NcLayerF), P, P, ctypes.POINTER(NcLayerWC),
+                                      P, P, ctypes.POINTER(NcLayerG), P, P, P, P,
+                                      ctypes.POINTER(NcLayerF), P, S, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -191,6 +221,17 @@ def gemm(dtype, layout, epilogue, M, N, K, A, lda, B, ldb, C, ldc, aux=None, acc
     p, n = _ws(ws)
     _check(L.nc_gemm(dtype, layout, epilogue, M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
                      _ptr(aux), int(accumulate), p, n, _stream()))
+    return ws
+
+
+def gemm_batched(dtype, layout, epilogue, batch, M, N, K, A, lda, a_bstride, B, ldb, b_bstride,
+                 C, ldc, c_bstride, aux=None, alpha=0.0, beta=1.0, ws=None):
+    if ws is None:
+        ws = alloc_workspace(256, A.device)
+    p, n = _ws(ws)
+    _check(lib().nc_gemm_batched(dtype, layout, epilogue, batch, M, N, K, _ptr(A), lda, a_bstride,
+                                 _ptr(B), ldb, b_bstride, _ptr(C), ldc, c_bstride, _ptr(aux),
+                                 float(alpha), float(beta), p, n, _stream()))
     return ws
 
 
@@ -299,3 +340,56 @@ class Step:
 
     def status(self) -> int:
         return get_device_status(self.ws)
+
+
+# Muon's published defaults (momentum 0.95, the quintic Newton-Schulz
+# coefficients, five steps); AdamW's betas and eps as in the AdamW paper.
+MUON_NS = (3.4445, -4.7750, 2.0315)
+
+
+class Optimizer:
+    """float32 master weights plus Muon + AdamW state for the parameters of a
+    Step.  step(t, lrm) applies nc_optimizer_step to the Step's gradients and
+    rewrites the Step's compute weights (bf16 or float) from the masters."""
+
+    def __init__(self, st: Step, lr_muon=0.02, momentum=0.95, lr_embed=0.1, lr_lm=0.01,
+                 betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0, ns=MUON_NS, ns_steps=5,
+                 masters: dict | None = None):
+        self.st = st
+        dev = st.device
+        src = masters if masters is not None else st.w
+        self.p = {k: torch.as_tensor(src[k]).to(device=dev, dtype=torch.float32).clone()
+                  for k in st.w}
+        self.state = {}
+        for k, v in self.p.items():
+            if k in ("wte", "w_lm"):
+                self.state[k] = {"m": torch.zeros_like(v), "v": torch.zeros_like(v)}
+            else:
+                self.state[k] = {"buf": torch.zeros_like(v)}
+        self.oc = NcOptConfig(lr_muon, momentum, lr_embed, lr_lm, betas[0], betas[1], eps,
+                              weight_decay, ns[0], ns[1], ns[2], ns_steps)
+        L = st.shape.depth
+        self.masters = (NcLayerF * L)(*[NcLayerF(*(self.p[f"{n}.{l}"].data_ptr()
+                                                   for n in ("w_qkv", "w_o", "w_fc", "w_proj")))
+                                        for l in range(L)])
+        self.copies = (NcLayerWC * L)(*[NcLayerWC(*(st.w[f"{n}.{l}"].data_ptr()
+                                                    for n in ("w_qkv", "w_o", "w_fc", "w_proj")))
+                                        for l in range(L)])
+        self.mom = (NcLayerF * L)(*[NcLayerF(*(self.state[f"{n}.{l}"]["buf"].data_ptr()
+                                               for n in ("w_qkv", "w_o", "w_fc", "w_proj")))
+                                    for l in range(L)])
+        nbytes = lib().nc_optimizer_workspace_bytes(ctypes.byref(st.cfg))
+        if nbytes == 0:
+            raise NcError(2, lib().nc_last_error_message().decode())
+        self.ws = alloc_workspace(nbytes, dev)
+
+    def step(self, t: int, lrm: float = 1.0) -> None:
+        st, p, s = self.st, self.p, self.state
+        wp, wn = _ws(self.ws)
+        _check(lib().nc_optimizer_step(
+            ctypes.byref(st.cfg), ctypes.byref(self.oc), int(t), float(lrm),
+            p["wte"].data_ptr(), p["w_lm"].data_ptr(), self.masters,
+            st.w["wte"].data_ptr(), st.w["w_lm"].data_ptr(), self.copies,
+            st.g["wte"].data_ptr(), st.g["w_lm"].data_ptr(), st.grads,
+            s["wte"]["m"].data_ptr(), s["wte"]["v"].data_ptr(), s["w_lm"]["m"].data_ptr(),
+            s["w_lm"]["v"].data_ptr(), self.mom, wp, wn, _stream(st.device)))

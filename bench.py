@@ -365,6 +365,30 @@ def run_ours(args, rank, world, local_rank):
             entry["gbs"] = amount * cnt / (tot / 1000.0) / 1e9
         kernels.append(entry)
 
+    # optimizer step (Muon + AdamW) on the step's gradients: time per step and
+    # the Newton-Schulz GEMM rate; not part of the fwd+bwd metric above
+    optim = None
+    if not args.no_optimizer:
+        o = nc.Optimizer(st)
+        for t in range(1, 3):
+            o.step(t, 1.0)
+        torch.cuda.synchronize()
+        n0 = nc.launch_count()
+        e0.record(stream)
+        for t in range(3, 3 + args.steps):
+            o.step(t, 1.0)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        o_ms = e0.elapsed_time(e1) / args.steps
+        ns_flops, adam_bytes = flops.optimizer_cost(shape)
+        optim = {"ms_per_step": o_ms, "launches_per_step": (nc.launch_count() - n0) / args.steps,
+                 "newton_schulz_flops": ns_flops, "adamw_bytes": adam_bytes,
+                 "newton_schulz_tflops_if_all_time": ns_flops / (o_ms / 1000.0) / 1e12,
+                 "note": "Muon for the block matrices (5 quintic Newton-Schulz steps, batched "
+                         "tcgen05 GEMMs), AdamW for wte and w_lm; fp32 masters and state"}
+        del o
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del st
@@ -392,7 +416,7 @@ def run_ours(args, rank, world, local_rank):
                               per_gpu * f_tok_causal / (peaks["bf16_tflops"] * 1e12),
                           "peak_source": peak_src},
            "loss": loss, "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
-           "e2e": e2e, "gpu_launches": launches, "clocks": clk}
+           "e2e": e2e, "gpu_launches": launches, "clocks": clk, "optimizer": optim}
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -407,6 +431,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-optimizer", action="store_true")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

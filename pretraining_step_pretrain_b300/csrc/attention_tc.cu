@@ -373,8 +373,8 @@ constexpr int DO_OFF = 32768;                // 32 KB
 constexpr int KVS = 4;                       // K/V ring stages
 constexpr int K_OFF = 65536;                 // KVS x 16 KB
 constexpr int V_OFF = K_OFF + KVS * 16384;   // KVS x 16 KB
-constexpr int DS_OFF = V_OFF + KVS * 16384;  // 16 KB ([128 rows][64 keys])
-constexpr int DL_OFF = DS_OFF + 16384;       // [2][128] fp32 halves of delta
+constexpr int DS_OFF = V_OFF + KVS * 16384;  // 2 x 16 KB ([128 rows][64 keys], by tile parity)
+constexpr int DL_OFF = DS_OFF + 2 * 16384;   // [2][128] fp32 halves of delta
 constexpr int BAR_OFF = DL_OFF + 1024;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 }  // namespace bdq
@@ -397,10 +397,10 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* kv_empty = bars + 1 + KVS;  // [KVS]
   uint64_t* s_full = bars + 1 + 2 * KVS;    // [2]
   uint64_t* s_free = bars + 3 + 2 * KVS;    // [2], one arrival per softmax warp
-  uint64_t* ds_full = bars + 5 + 2 * KVS;   // one arrival per softmax warp
-  uint64_t* dq_done = bars + 6 + 2 * KVS;
-  uint64_t* drain = bars + 7 + 2 * KVS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * KVS);
+  uint64_t* ds_full = bars + 5 + 2 * KVS;   // [2] by tile parity, one arrival per softmax warp
+  uint64_t* dq_done = bars + 7 + 2 * KVS;   // [2] by tile parity
+  uint64_t* drain = bars + 9 + 2 * KVS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * KVS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -421,8 +421,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], NSW);
     }
-    mbar_init(ds_full, NSW);
-    mbar_init(dq_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ds_full[i], NSW);
+      mbar_init(&dq_done[i], 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -496,15 +498,15 @@ __global__ void __launch_bounds__(NT, 1)
     if (ok) ok = issue_s(0);
     for (int j = 0; ok && j < nkv; ++j) {
       if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-      const int ks = j % KVS;
-      if (!sync.wait(ds_full, j & 1)) { ok = false; break; }
+      const int ks = j % KVS, db = j & 1;
+      if (!sync.wait(&ds_full[db], (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint32_t sK = smem_u32(smem + K_OFF + ks * 16384);
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, desc_k_atoms(sDS, kk, QATOM), desc_mn_blocks(sK, kk, KATOM), idQ,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(dq_done);
+        umma_bf16(tmem + 256, desc_k_atoms(sDS + db * 16384, kk, QATOM),
+                  desc_mn_blocks(sK, kk, KATOM), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&dq_done[db]);
       umma_commit(&kv_empty[ks]);
     }
     if ((!ok || *abort_flag) && issued) {
@@ -572,16 +574,18 @@ __global__ void __launch_bounds__(NT, 1)
         if (need_mask && (!valid || key0 + i > t)) p = 0.f;
         s[i] = p * (dp[i] - dl);
       }
-      if (j > 0) {  // the dQ MMA of the previous tile has read the dS buffer
-        if (!sync.wait(dq_done, (j - 1) & 1)) { ok = false; break; }
+      const int db = j & 1;
+      if (j > 1) {  // the dQ MMA of tile j - 2 has read this dS buffer
+        if (!sync.wait(&dq_done[db], ((j >> 1) - 1) & 1)) { ok = false; break; }
       }
-      store_half_row_atom(smem + DS_OFF, row, half * 4, s);
+      store_half_row_atom(smem + DS_OFF + db * 16384, row, half * 4, s);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&ds_full[db]);
     }
-    if (ok && sync.wait(dq_done, (nkv - 1) & 1)) {
+    // dQ MMAs complete in issue order: the last one done means all are.
+    if (ok && sync.wait(&dq_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       bf16* qrow = dq + ((long)b * T + t) * ldq + (long)(r % H) * HD;
@@ -611,12 +615,12 @@ constexpr int KATOM = 16384;   // [128 keys][64]
 constexpr int QATOM = 8192;    // [64 rows][64]
 constexpr int K_OFF = 0;                      // 32 KB
 constexpr int V_OFF = 32768;                  // 32 KB
-constexpr int QS = 4;                         // Q / dO ring stages
+constexpr int QS = 3;                         // Q / dO ring stages
 constexpr int Q_OFF = 65536;                  // QS x 16 KB
 constexpr int DO_OFF = Q_OFF + QS * 16384;    // QS x 16 KB
-constexpr int PT_OFF = DO_OFF + QS * 16384;   // 16 KB ([128 keys][64 rows])
-constexpr int DST_OFF = PT_OFF + 16384;       // 16 KB
-constexpr int INFO_OFF = DST_OFF + 16384;     // [2][64] x (lse2, delta, tok)
+constexpr int PT_OFF = DO_OFF + QS * 16384;   // 2 x 16 KB ([128 keys][64 rows], by tile parity)
+constexpr int DST_OFF = PT_OFF + 2 * 16384;   // 2 x 16 KB
+constexpr int INFO_OFF = DST_OFF + 2 * 16384; // [2][64] x (lse2, delta, tok)
 constexpr int BAR_OFF = INFO_OFF + 2 * 64 * 12 + 128;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 static_assert(SMEM <= 232448, "dK/dV pass shared memory exceeds 227 KB");
@@ -640,12 +644,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* q_empty = bars + 1 + QS;    // [QS]
   uint64_t* s_full = bars + 1 + 2 * QS;    // [2]
   uint64_t* s_free = bars + 3 + 2 * QS;    // [2], one arrival per softmax warp
-  uint64_t* p_full = bars + 5 + 2 * QS;    // one arrival per softmax warp
-  uint64_t* pd_done = bars + 6 + 2 * QS;
-  uint64_t* drain = bars + 7 + 2 * QS;
-  uint64_t* info_full = bars + 8 + 2 * QS;   // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 10 + 2 * QS;  // [2], one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12 + 2 * QS);
+  uint64_t* p_full = bars + 5 + 2 * QS;    // [2] by tile parity, one arrival per softmax warp
+  uint64_t* pd_done = bars + 7 + 2 * QS;   // [2] by tile parity
+  uint64_t* drain = bars + 9 + 2 * QS;
+  uint64_t* info_full = bars + 10 + 2 * QS;  // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 12 + 2 * QS;  // [2], one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14 + 2 * QS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][64]
   float* info_dl = info_lse + 2 * 64;                                 // [2][64]
@@ -668,8 +672,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], NSW);
     }
-    mbar_init(p_full, NSW);
-    mbar_init(pd_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], NSW);
+      mbar_init(&pd_done[i], 1);
+    }
     mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&info_full[i], 32);
@@ -764,20 +770,20 @@ __global__ void __launch_bounds__(NT, 1)
     if (ok) ok = issue_s(0);
     for (int i = 0; ok && i < n_rt; ++i) {
       if (i + 1 < n_rt && !issue_s(i + 1)) { ok = false; break; }
-      const int qs = i % QS;
-      if (!sync.wait(p_full, i & 1)) { ok = false; break; }
+      const int qs = i % QS, pb = i & 1;
+      if (!sync.wait(&p_full[pb], (i >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
       const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk)
-        umma_bf16(tmem + 256, desc_k_atoms(sPt, kk, KATOM), desc_mn_blocks(sDO, kk, QATOM), idG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 256, desc_k_atoms(sPt + pb * 16384, kk, KATOM),
+                  desc_mn_blocks(sDO, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk)
-        umma_bf16(tmem + 384, desc_k_atoms(sdSt, kk, KATOM), desc_mn_blocks(sQ, kk, QATOM), idG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(pd_done);
+        umma_bf16(tmem + 384, desc_k_atoms(sdSt + pb * 16384, kk, KATOM),
+                  desc_mn_blocks(sQ, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&pd_done[pb]);
       umma_commit(&q_empty[qs]);
     }
     if ((!ok || *abort_flag) && issued) {
@@ -830,17 +836,19 @@ __global__ void __launch_bounds__(NT, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&info_free[st]);
-      if (i > 0) {  // dV/dK MMAs of the previous tile have read P^T, dS^T
-        if (!sync.wait(pd_done, (i - 1) & 1)) { ok = false; break; }
+      const int pb = i & 1;
+      if (i > 1) {  // dV/dK MMAs of tile i - 2 have read this P^T, dS^T buffer
+        if (!sync.wait(&pd_done[pb], ((i >> 1) - 1) & 1)) { ok = false; break; }
       }
-      store_half_row_atom(smem + PT_OFF, krow, half * 4, s);
-      store_half_row_atom(smem + DST_OFF, krow, half * 4, dp);
+      store_half_row_atom(smem + PT_OFF + pb * 16384, krow, half * 4, s);
+      store_half_row_atom(smem + DST_OFF + pb * 16384, krow, half * 4, dp);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[pb]);
     }
-    if (ok && n_rt > 0 && sync.wait(pd_done, (n_rt - 1) & 1)) {
+    // MMAs complete in issue order: the last tile's done means all are.
+    if (ok && n_rt > 0 && sync.wait(&pd_done[(n_rt - 1) & 1], ((n_rt - 1) >> 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       const bool valid = key < T;

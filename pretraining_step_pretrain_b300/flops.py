@@ -27,3 +27,20 @@ def flops_per_token(shape, seq: int, causal_actual: bool = False, n_kv_head: int
     dense = 6 * (L * block_params(shape, n_kv_head) + V * d)
     attn = (6 if causal_actual else 12) * L * H * h * seq
     return float(dense + attn)
+
+
+def optimizer_cost(shape, ns_steps: int = 5) -> tuple[float, float]:
+    """(Newton-Schulz FLOPs, AdamW bytes) of one optimizer step.
+
+    Each block matrix (r x c, wide orientation m = min, n = max) costs, per
+    Newton-Schulz step, 2 m^2 n (A = X X^T) + 2 m^3 (A A) + 2 m^2 n (B X).
+    AdamW reads the master, gradient and both moments (fp32) and writes the
+    master, both moments and the bf16 compute copy: 30 bytes per element of
+    the embedding and of the LM head."""
+    d, H, h, f = shape.d_model, shape.n_head, shape.head_dim, shape.d_mlp
+    mats = [((H + 2) * h, d), (d, H * h), (f, d), (d, f)]
+    per_layer = 0
+    for r, c in mats:
+        m, n = min(r, c), max(r, c)
+        per_layer += ns_steps * (4 * m * m * n + 2 * m ** 3)
+    return float(shape.depth * per_layer), float(2 * shape.vocab * d * 30)

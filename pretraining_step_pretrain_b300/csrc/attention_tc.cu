@@ -79,6 +79,32 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// D (+)= A B^T with the A operand (M rows = TMEM lanes, 16 K values packed
+// two bf16 per 32-bit column) read from tensor memory at a_tmem.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 64 bf16 of one row (a 128-byte global slice) into this thread's TMEM lane
+// as 32 columns, element 2i in the low half of column i.
+__device__ __forceinline__ void row64_to_tmem(uint32_t taddr, const bf16* src, bool valid) {
+  float v[32];
+  uint4 q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    q[i] = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(q);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
+  tmem_st_32cols(taddr, v);
+}
+
 // Store 32 fp32 values as bf16 to global (64 contiguous bytes).
 __device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32], float scale) {
 #pragma unroll
@@ -361,29 +387,33 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ======================================================================
-// backward, dQ pass: 128 packed query rows per CTA, 64-key tiles.  Also
-// writes delta = rowsum(dO * O) for the dK/dV pass.
+// backward, dQ pass: 128 packed query rows per CTA against 128-key tiles.
+// Also writes delta = rowsum(dO * O) for the dK/dV pass.  Q and dO, the same
+// for every key tile, sit in tensor memory as the A operands of S = Q K^T
+// and dP = dO V^T, so shared memory only streams K and V.  S and dP (128
+// columns each) are single-buffered: the softmax warps copy them to
+// registers and release them at once, so the next tile's MMAs start while
+// dS is being formed.  Every MMA is N = 128 wide (narrower ones run at
+// ~60% of the tensor rate: their shared-memory operand traffic per FLOP is
+// higher).
 // ======================================================================
 namespace bdq {
-constexpr int BQ = 128, BKV = 64;
-constexpr int QATOM = 16384;   // [128 rows][64]
-constexpr int KATOM = 8192;    // [64 keys][64]
-constexpr int Q_OFF = 0;                     // 32 KB
-constexpr int DO_OFF = 32768;                // 32 KB
-constexpr int KVS = 4;                       // K/V ring stages
-constexpr int K_OFF = 65536;                 // KVS x 16 KB
-constexpr int V_OFF = K_OFF + KVS * 16384;   // KVS x 16 KB
-constexpr int DS_OFF = V_OFF + KVS * 16384;  // 2 x 16 KB ([128 rows][64 keys], by tile parity)
-constexpr int DL_OFF = DS_OFF + 2 * 16384;   // [2][128] fp32 halves of delta
+constexpr int BQ = 128, BKV = 128;
+constexpr int ATOM = 16384;                  // [128 rows][64] bf16
+constexpr int KVS = 2;                       // K/V ring stages (64 KB each)
+constexpr int K_OFF = 0;                     // KVS x 32 KB ([128 keys][128 dims] = 2 atoms)
+constexpr int V_OFF = K_OFF + KVS * 32768;   // KVS x 32 KB
+constexpr int DS_OFF = V_OFF + KVS * 32768;  // 2 x 32 KB ([128 rows][128 keys], by tile parity)
+constexpr int DL_OFF = DS_OFF + 2 * 32768;   // [2][128] fp32 halves of delta
 constexpr int BAR_OFF = DL_OFF + 1024;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
+static_assert(SMEM <= 232448, "dQ pass shared memory exceeds 227 KB");
 }  // namespace bdq
 
 __global__ void __launch_bounds__(NT, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                          const __grid_constant__ CUtensorMap tmDO,
-                          const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ o,
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
+                          const bf16* __restrict__ o,
                           const bf16* __restrict__ dout, const float* __restrict__ lse,
                           bf16* __restrict__ dq, long ldq, float* __restrict__ delta, int T, int H,
                           int* err, long long timeout_ns) {
@@ -392,15 +422,15 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* q_full = bars + 0;
+  uint64_t* q_full = bars + 0;          // Q and dO in tensor memory (softmax warps)
   uint64_t* kv_full = bars + 1;         // [KVS]
   uint64_t* kv_empty = bars + 1 + KVS;  // [KVS]
-  uint64_t* s_full = bars + 1 + 2 * KVS;    // [2]
-  uint64_t* s_free = bars + 3 + 2 * KVS;    // [2], one arrival per softmax warp
-  uint64_t* ds_full = bars + 5 + 2 * KVS;   // [2] by tile parity, one arrival per softmax warp
-  uint64_t* dq_done = bars + 7 + 2 * KVS;   // [2] by tile parity
-  uint64_t* drain = bars + 9 + 2 * KVS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * KVS);
+  uint64_t* s_full = bars + 1 + 2 * KVS;    // S and dP of the tile ready
+  uint64_t* s_free = bars + 2 + 2 * KVS;    // copied out, one arrival per softmax warp
+  uint64_t* ds_full = bars + 3 + 2 * KVS;   // [2] by tile parity, one arrival per softmax warp
+  uint64_t* dq_done = bars + 5 + 2 * KVS;   // [2] by tile parity
+  uint64_t* drain = bars + 7 + 2 * KVS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * KVS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -412,15 +442,13 @@ __global__ void __launch_bounds__(NT, 1)
   const int nkv = t_last / BKV + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, NSW);
     for (int i = 0; i < KVS; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSW);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, NSW);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ds_full[i], NSW);
       mbar_init(&dq_done[i], 1);
@@ -438,76 +466,73 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const CtaSync sync{abort_flag, err, timeout_ns};
-  // TMEM columns: S[st] at 64 st, dP[st] at 128 + 64 st, dQ at 256.
+  // TMEM columns: S at 0, dP at 128, dQ at 256, Q at 384, dO at 448 (bf16 pairs).
 
   if (warp == 0 && lane == 0) {
-    int armed[1 + KVS];
-    for (int i = 0; i < 1 + KVS; ++i) armed[i] = -1;
-    mbar_arrive_expect_tx(q_full, 4 * QATOM);
-    tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, (int)r0, b);
-    tma_load_3d(smem + Q_OFF + QATOM, &tmQ, q_full, 64, (int)r0, b);
-    tma_load_3d(smem + DO_OFF, &tmDO, q_full, 0, (int)r0, b);
-    tma_load_3d(smem + DO_OFF + QATOM, &tmDO, q_full, 64, (int)r0, b);
-    armed[0] = 0;
+    // ------------------------------------------------ TMA producer (K, V)
+    int armed[KVS];
+    for (int i = 0; i < KVS; ++i) armed[i] = -1;
     for (int j = 0; j < nkv; ++j) {
       const int ks = j % KVS;
       const uint32_t kph = (j / KVS) & 1;
       if (!sync.wait(&kv_empty[ks], kph ^ 1u)) break;
-      mbar_arrive_expect_tx(&kv_full[ks], 4 * KATOM);
-      tma_load_3d(smem + K_OFF + ks * 16384, &tmK, &kv_full[ks], 0, j * BKV, b);
-      tma_load_3d(smem + K_OFF + ks * 16384 + KATOM, &tmK, &kv_full[ks], 64, j * BKV, b);
-      tma_load_3d(smem + V_OFF + ks * 16384, &tmV, &kv_full[ks], 0, j * BKV, b);
-      tma_load_3d(smem + V_OFF + ks * 16384 + KATOM, &tmV, &kv_full[ks], 64, j * BKV, b);
-      armed[1 + ks] = (int)kph;
+      mbar_arrive_expect_tx(&kv_full[ks], 4 * ATOM);
+      tma_load_3d(smem + K_OFF + ks * 32768, &tmK, &kv_full[ks], 0, j * BKV, b);
+      tma_load_3d(smem + K_OFF + ks * 32768 + ATOM, &tmK, &kv_full[ks], 64, j * BKV, b);
+      tma_load_3d(smem + V_OFF + ks * 32768, &tmV, &kv_full[ks], 0, j * BKV, b);
+      tma_load_3d(smem + V_OFF + ks * 32768 + ATOM, &tmV, &kv_full[ks], 64, j * BKV, b);
+      armed[ks] = (int)kph;
     }
     if (*abort_flag) {
       int none = 0;
-      if (armed[0] >= 0) mbar_wait_bounded(q_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
       for (int i = 0; i < KVS; ++i)
-        if (armed[1 + i] >= 0)
-          mbar_wait_bounded(&kv_full[i], (uint32_t)armed[1 + i], &none, err, SITE_ATTN,
+        if (armed[i] >= 0)
+          mbar_wait_bounded(&kv_full[i], (uint32_t)armed[i], &none, err, SITE_ATTN,
                             timeout_ns / 8);
     }
   } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idQ = idesc_bf16_mn(false, true, BQ, HD);
-    const uint32_t sQ = smem_u32(smem + Q_OFF), sDO = smem_u32(smem + DO_OFF);
     const uint32_t sDS = smem_u32(smem + DS_OFF);
     bool ok = sync.wait(q_full, 0), issued = false;
+    // S(j) and dP(j) into the single TMEM buffer once tile j - 1's copies are out.
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;  // TMEM S / dP buffer
-      const uint32_t ph = (j >> 1) & 1;
-      const int ks = j % KVS;  // shared-memory K/V stage
-      if (!sync.wait(&kv_full[ks], (j / KVS) & 1) || !sync.wait(&s_free[st], ph ^ 1u))
-        return false;
+      const int ks = j % KVS;
+      if (!sync.wait(&kv_full[ks], (j / KVS) & 1)) return false;
+      if (j > 0 && !sync.wait(s_free, (j - 1) & 1)) return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + ks * 16384);
-      const uint32_t sV = smem_u32(smem + V_OFF + ks * 16384);
+      const uint32_t sK = smem_u32(smem + K_OFF + ks * 32768);
+      const uint32_t sV = smem_u32(smem + V_OFF + ks * 32768);
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + st * 64, desc_k_atoms(sQ, kk, QATOM), desc_k_atoms(sK, kk, KATOM), idS,
-                  kk > 0 ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + 128 + st * 64, desc_k_atoms(sDO, kk, QATOM),
-                  desc_k_atoms(sV, kk, KATOM), idS, kk > 0 ? 1u : 0u);
-      umma_commit(&s_full[st]);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        umma_bf16_tmem_a(tmem + 0, tmem + 384 + kk * 8, desc_k_atoms(sK, kk, ATOM), idS,
+                         kk > 0 ? 1u : 0u);
+        umma_bf16_tmem_a(tmem + 128, tmem + 448 + kk * 8, desc_k_atoms(sV, kk, ATOM), idS,
+                         kk > 0 ? 1u : 0u);
+      }
+      umma_commit(s_full);
       issued = true;
+      return true;
+    };
+    // dQ += dS(j) K(j)
+    auto issue_dq = [&](int j) -> bool {
+      const int ks = j % KVS, db = j & 1;
+      if (!sync.wait(&ds_full[db], (j >> 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t sK = smem_u32(smem + K_OFF + ks * 32768);
+#pragma unroll
+      for (int kk = 0; kk < BKV / 16; ++kk)
+        umma_bf16(tmem + 256, desc_k_atoms(sDS + db * 32768, kk, ATOM),
+                  desc_mn_blocks(sK, kk, ATOM), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&dq_done[db]);
+      umma_commit(&kv_empty[ks]);
       return true;
     };
     if (ok) ok = issue_s(0);
     for (int j = 0; ok && j < nkv; ++j) {
       if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-      const int ks = j % KVS, db = j & 1;
-      if (!sync.wait(&ds_full[db], (j >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + ks * 16384);
-#pragma unroll
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, desc_k_atoms(sDS + db * 16384, kk, QATOM),
-                  desc_mn_blocks(sK, kk, KATOM), idQ, (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&dq_done[db]);
-      umma_commit(&kv_empty[ks]);
+      if (!issue_dq(j)) { ok = false; break; }
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
@@ -515,8 +540,9 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
-    // Softmax warps: warp 4 + 4 half + quarter owns packed rows 32 quarter ..
-    // 32 quarter + 31 (its TMEM lanes) and key columns 32 half .. 32 half + 31.
+    // ------------------------------------------------ softmax warps
+    // Warp 4 + 4 half + quarter owns packed rows 32 quarter .. 32 quarter + 31
+    // (its TMEM lanes) and key columns 64 half .. 64 half + 63 of each tile.
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
@@ -546,6 +572,13 @@ __global__ void __launch_bounds__(NT, 1)
       }
       lse2 = lse[grow] * kLog2e;
     }
+    // This thread's halves of the Q and dO rows into tensor memory (the A
+    // operands of every S and dP MMA); rows past the sequence are zero.
+    row64_to_tmem(tmem + lane_off + 384 + half * 32, q + grow * HD + half * 64, valid);
+    row64_to_tmem(tmem + lane_off + 448 + half * 32, dout + grow * HD + half * 64, valid);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_full);
     dl_part[half * 128 + row] = dl;
     asm volatile("bar.sync 1, %0;" ::"n"(NSW * 32) : "memory");  // the 8 softmax warps
     dl = dl_part[row] + dl_part[128 + row];
@@ -556,20 +589,21 @@ __global__ void __launch_bounds__(NT, 1)
     const bool rows_ragged = r0 + BQ > TH;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
+      if (!sync.wait(s_full, j & 1)) { ok = false; break; }
       tc_fence_after();
-      float s[32], dp[32];
-      tmem_ld_32cols(tmem + lane_off + st * 64 + half * 32, s);
-      tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + half * 32, dp);
+      float s[64], dp[64];
+      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(s));
+      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+      tmem_ld_32cols(tmem + lane_off + 128 + half * 64, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld_32cols(tmem + lane_off + 128 + half * 64 + 32,
+                     *reinterpret_cast<float(*)[32]>(dp + 32));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-      const int key0 = j * BKV + half * 32;
-      const bool need_mask = rows_ragged || key0 + 31 > t0;
+      if (lane == 0) mbar_arrive(s_free);
+      const int key0 = j * BKV + half * 64;
+      const bool need_mask = rows_ragged || key0 + 63 > t0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         float p = ex2(fmaf(s[i], sl2, -lse2));
         if (need_mask && (!valid || key0 + i > t)) p = 0.f;
         s[i] = p * (dp[i] - dl);
@@ -578,7 +612,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (j > 1) {  // the dQ MMA of tile j - 2 has read this dS buffer
         if (!sync.wait(&dq_done[db], ((j >> 1) - 1) & 1)) { ok = false; break; }
       }
-      store_half_row_atom(smem + DS_OFF + db * 16384, row, half * 4, s);
+      store_row_atom(smem + DS_OFF + db * 32768 + half * ATOM, row, s);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -755,14 +789,14 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
       const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
+      // S^T and dP^T are independent chains: alternate their k-steps.
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
+      for (int kk = 0; kk < HD / 16; ++kk) {
         umma_bf16(tmem + st * 64, desc_k_atoms(sK, kk, KATOM), desc_k_atoms(sQ, kk, QATOM), idS,
                   kk > 0 ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
         umma_bf16(tmem + 128 + st * 64, desc_k_atoms(sV, kk, KATOM),
                   desc_k_atoms(sDO, kk, QATOM), idS, kk > 0 ? 1u : 0u);
+      }
       umma_commit(&s_full[st]);
       issued = true;
       return true;
@@ -775,14 +809,14 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
       const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
+      // dV and dK: independent chains, alternated.
 #pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk)
+      for (int kk = 0; kk < BQ / 16; ++kk) {
         umma_bf16(tmem + 256, desc_k_atoms(sPt + pb * 16384, kk, KATOM),
                   desc_mn_blocks(sDO, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk)
         umma_bf16(tmem + 384, desc_k_atoms(sdSt + pb * 16384, kk, KATOM),
                   desc_mn_blocks(sQ, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
+      }
       umma_commit(&pd_done[pb]);
       umma_commit(&q_empty[qs]);
     }
@@ -919,13 +953,12 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   }
   const long TH = (long)T * H;
   CUtensorMap mq, mdo, mk, mv;
-  if (!map3(&mq, q, TH, B, bdq::BQ) || !map3(&mdo, dout, TH, B, bdq::BQ) ||
-      !map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV))
+  if (!map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV))
     return cudaErrorInvalidValue;
   dim3 gq(B, (unsigned)((TH + bdq::BQ - 1) / bdq::BQ));
   attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
-      mq, mdo, mk, mv, (const nc::bf16*)o, (const nc::bf16*)dout, lse, (nc::bf16*)dq, ldq, delta,
-      T, H, ctx.err, ctx.timeout_ns);
+      mk, mv, (const nc::bf16*)q, (const nc::bf16*)o, (const nc::bf16*)dout, lse, (nc::bf16*)dq,
+      ldq, delta, T, H, ctx.err, ctx.timeout_ns);
   note_launch(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

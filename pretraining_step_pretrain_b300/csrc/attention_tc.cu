@@ -640,31 +640,31 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ======================================================================
-// backward, dK/dV pass: 128 keys per CTA, 64-row query tiles over every
-// packed row that can see them (all heads: the MQA head sum).
+// backward, dK/dV pass: 128 keys per CTA against 128-row query tiles over
+// every packed row that can see them (all heads: the MQA head sum).  K and
+// V, the same for every query tile, sit in tensor memory as the A operands
+// of S^T = K Q^T and dP^T = V dO^T; one 128-column score buffer holds S^T,
+// is copied out, then holds dP^T.  dV += P^T dO and dK += dS^T Q accumulate
+// in tensor memory; every MMA is N = 128 wide.
 // ======================================================================
 namespace bkv {
-constexpr int BKV = 128, BQ = 64;
-constexpr int KATOM = 16384;   // [128 keys][64]
-constexpr int QATOM = 8192;    // [64 rows][64]
-constexpr int K_OFF = 0;                      // 32 KB
-constexpr int V_OFF = 32768;                  // 32 KB
-constexpr int QS = 3;                         // Q / dO ring stages
-constexpr int Q_OFF = 65536;                  // QS x 16 KB
-constexpr int DO_OFF = Q_OFF + QS * 16384;    // QS x 16 KB
-constexpr int PT_OFF = DO_OFF + QS * 16384;   // 2 x 16 KB ([128 keys][64 rows], by tile parity)
-constexpr int DST_OFF = PT_OFF + 2 * 16384;   // 2 x 16 KB
-constexpr int INFO_OFF = DST_OFF + 2 * 16384; // [2][64] x (lse2, delta, tok)
-constexpr int BAR_OFF = INFO_OFF + 2 * 64 * 12 + 128;
+constexpr int BKV = 128, BQ = 128;
+constexpr int ATOM = 16384;                   // [128 rows][64] bf16
+constexpr int QS = 2;                         // Q / dO ring stages (64 KB each)
+constexpr int Q_OFF = 0;                      // QS x 32 KB
+constexpr int DO_OFF = Q_OFF + QS * 32768;    // QS x 32 KB
+constexpr int PT_OFF = DO_OFF + QS * 32768;   // 32 KB ([128 keys][128 rows])
+constexpr int DST_OFF = PT_OFF + 32768;       // 32 KB
+constexpr int INFO_OFF = DST_OFF + 32768;     // [2][128] x (lse2, delta, tok)
+constexpr int BAR_OFF = INFO_OFF + 2 * 128 * 12 + 128;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 static_assert(SMEM <= 232448, "dK/dV pass shared memory exceeds 227 KB");
 }  // namespace bkv
 
 __global__ void __launch_bounds__(NT, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                            const __grid_constant__ CUtensorMap tmDO,
-                            const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV, const float* __restrict__ lse,
+                            const __grid_constant__ CUtensorMap tmDO, const bf16* __restrict__ kg,
+                            const bf16* __restrict__ vg, const float* __restrict__ lse,
                             const float* __restrict__ delta, bf16* __restrict__ dk, long ldk,
                             bf16* __restrict__ dv, long ldv, int T, int H, int* err,
                             long long timeout_ns) {
@@ -673,21 +673,21 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;          // [QS]
-  uint64_t* q_empty = bars + 1 + QS;    // [QS]
-  uint64_t* s_full = bars + 1 + 2 * QS;    // [2]
-  uint64_t* s_free = bars + 3 + 2 * QS;    // [2], one arrival per softmax warp
-  uint64_t* p_full = bars + 5 + 2 * QS;    // [2] by tile parity, one arrival per softmax warp
-  uint64_t* pd_done = bars + 7 + 2 * QS;   // [2] by tile parity
-  uint64_t* drain = bars + 9 + 2 * QS;
-  uint64_t* info_full = bars + 10 + 2 * QS;  // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 12 + 2 * QS;  // [2], one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14 + 2 * QS);
+  uint64_t* kv_full = bars + 0;             // K, V in tensor memory (softmax warps)
+  uint64_t* q_full = bars + 1;              // [QS]
+  uint64_t* q_empty = bars + 1 + QS;        // [QS]
+  uint64_t* sc_full = bars + 1 + 2 * QS;    // score buffer holds S^T, then dP^T
+  uint64_t* sc_free = bars + 2 + 2 * QS;    // copied out, one arrival per softmax warp
+  uint64_t* p_full = bars + 3 + 2 * QS;     // P^T, dS^T stored, one arrival per softmax warp
+  uint64_t* pd_done = bars + 4 + 2 * QS;    // dV, dK MMAs of the tile done
+  uint64_t* drain = bars + 5 + 2 * QS;
+  uint64_t* info_full = bars + 6 + 2 * QS;  // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 8 + 2 * QS;  // [2], one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * QS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][64]
-  float* info_dl = info_lse + 2 * 64;                                 // [2][64]
-  int* info_tok = reinterpret_cast<int*>(info_dl + 2 * 64);           // [2][64]
+  float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][128]
+  float* info_dl = info_lse + 2 * 128;                                // [2][128]
+  int* info_tok = reinterpret_cast<int*>(info_dl + 2 * 128);          // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
@@ -697,19 +697,15 @@ __global__ void __launch_bounds__(NT, 1)
   const int n_rt = (int)((TH + BQ - 1) / BQ - rt0);
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
+    mbar_init(kv_full, NSW);
     for (int i = 0; i < QS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSW);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&p_full[i], NSW);
-      mbar_init(&pd_done[i], 1);
-    }
+    mbar_init(sc_full, 1);
+    mbar_init(sc_free, NSW);
+    mbar_init(p_full, NSW);
+    mbar_init(pd_done, 1);
     mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&info_full[i], 32);
@@ -727,7 +723,7 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const CtaSync sync{abort_flag, err, timeout_ns};
-  // TMEM columns: St[st] at 64 st, dPt[st] at 128 + 64 st, dV at 256, dK at 384.
+  // TMEM columns: score at 0, dV at 128, dK at 256, K at 384, V at 448 (bf16 pairs).
 
   if (warp == 3) {
     // ------------------------------------------------ per-row data of each query tile
@@ -738,162 +734,181 @@ __global__ void __launch_bounds__(NT, 1)
       for (int c = lane; c < BQ; c += 32) {
         const long rr = (rt0 + i) * BQ + c;
         const bool v = rr < TH;
-        info_lse[st * 64 + c] = v ? lse[(long)b * TH + rr] * kLog2e : 0.f;
-        info_dl[st * 64 + c] = v ? delta[(long)b * TH + rr] : 0.f;
-        info_tok[st * 64 + c] = v ? (int)(rr / H) : -1;
+        info_lse[st * 128 + c] = v ? lse[(long)b * TH + rr] * kLog2e : 0.f;
+        info_dl[st * 128 + c] = v ? delta[(long)b * TH + rr] : 0.f;
+        info_tok[st * 128 + c] = v ? (int)(rr / H) : -1;
       }
       mbar_arrive(&info_full[st]);
     }
   }
 
   if (warp == 0 && lane == 0) {
-    int armed[1 + QS];
-    for (int i = 0; i < 1 + QS; ++i) armed[i] = -1;
-    mbar_arrive_expect_tx(kv_full, 4 * KATOM);
-    tma_load_3d(smem + K_OFF, &tmK, kv_full, 0, j0, b);
-    tma_load_3d(smem + K_OFF + KATOM, &tmK, kv_full, 64, j0, b);
-    tma_load_3d(smem + V_OFF, &tmV, kv_full, 0, j0, b);
-    tma_load_3d(smem + V_OFF + KATOM, &tmV, kv_full, 64, j0, b);
-    armed[0] = 0;
+    // ------------------------------------------------ TMA producer (Q, dO)
+    int armed[QS];
+    for (int i = 0; i < QS; ++i) armed[i] = -1;
     for (int i = 0; i < n_rt; ++i) {
       const int qs = i % QS;
       const uint32_t qph = (i / QS) & 1;
       const int rr = (int)((rt0 + i) * BQ);
       if (!sync.wait(&q_empty[qs], qph ^ 1u)) break;
-      mbar_arrive_expect_tx(&q_full[qs], 4 * QATOM);
-      tma_load_3d(smem + Q_OFF + qs * 16384, &tmQ, &q_full[qs], 0, rr, b);
-      tma_load_3d(smem + Q_OFF + qs * 16384 + QATOM, &tmQ, &q_full[qs], 64, rr, b);
-      tma_load_3d(smem + DO_OFF + qs * 16384, &tmDO, &q_full[qs], 0, rr, b);
-      tma_load_3d(smem + DO_OFF + qs * 16384 + QATOM, &tmDO, &q_full[qs], 64, rr, b);
-      armed[1 + qs] = (int)qph;
+      mbar_arrive_expect_tx(&q_full[qs], 4 * ATOM);
+      tma_load_3d(smem + Q_OFF + qs * 32768, &tmQ, &q_full[qs], 0, rr, b);
+      tma_load_3d(smem + Q_OFF + qs * 32768 + ATOM, &tmQ, &q_full[qs], 64, rr, b);
+      tma_load_3d(smem + DO_OFF + qs * 32768, &tmDO, &q_full[qs], 0, rr, b);
+      tma_load_3d(smem + DO_OFF + qs * 32768 + ATOM, &tmDO, &q_full[qs], 64, rr, b);
+      armed[qs] = (int)qph;
     }
     if (*abort_flag) {
       int none = 0;
-      if (armed[0] >= 0) mbar_wait_bounded(kv_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
       for (int i = 0; i < QS; ++i)
-        if (armed[1 + i] >= 0)
-          mbar_wait_bounded(&q_full[i], (uint32_t)armed[1 + i], &none, err, SITE_ATTN,
+        if (armed[i] >= 0)
+          mbar_wait_bounded(&q_full[i], (uint32_t)armed[i], &none, err, SITE_ATTN,
                             timeout_ns / 8);
     }
   } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    // Per query tile i: S^T(i); dV, dK of tile i - 1; dP^T(i).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
     constexpr uint32_t idG = idesc_bf16_mn(false, true, BKV, HD);
-    const uint32_t sK = smem_u32(smem + K_OFF), sV = smem_u32(smem + V_OFF);
     const uint32_t sPt = smem_u32(smem + PT_OFF), sdSt = smem_u32(smem + DST_OFF);
     bool ok = sync.wait(kv_full, 0), issued = false;
-    auto issue_s = [&](int i) -> bool {
-      const int st = i & 1;  // TMEM S^T / dP^T buffer
-      const uint32_t ph = (i >> 1) & 1;
-      const int qs = i % QS;  // shared-memory Q / dO stage
-      if (!sync.wait(&q_full[qs], (i / QS) & 1) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
+    auto issue_grads = [&](int i) -> bool {  // dV += P^T dO, dK += dS^T Q of tile i
+      const int qs = i % QS;
+      if (!sync.wait(p_full, i & 1)) return false;
       tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
-      // S^T and dP^T are independent chains: alternate their k-steps.
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        umma_bf16(tmem + st * 64, desc_k_atoms(sK, kk, KATOM), desc_k_atoms(sQ, kk, QATOM), idS,
-                  kk > 0 ? 1u : 0u);
-        umma_bf16(tmem + 128 + st * 64, desc_k_atoms(sV, kk, KATOM),
-                  desc_k_atoms(sDO, kk, QATOM), idS, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(&s_full[st]);
-      issued = true;
-      return true;
-    };
-    if (ok) ok = issue_s(0);
-    for (int i = 0; ok && i < n_rt; ++i) {
-      if (i + 1 < n_rt && !issue_s(i + 1)) { ok = false; break; }
-      const int qs = i % QS, pb = i & 1;
-      if (!sync.wait(&p_full[pb], (i >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 16384);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 16384);
-      // dV and dK: independent chains, alternated.
+      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 32768);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 32768);
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk) {
-        umma_bf16(tmem + 256, desc_k_atoms(sPt + pb * 16384, kk, KATOM),
-                  desc_mn_blocks(sDO, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(tmem + 384, desc_k_atoms(sdSt + pb * 16384, kk, KATOM),
-                  desc_mn_blocks(sQ, kk, QATOM), idG, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 128, desc_k_atoms(sPt, kk, ATOM), desc_mn_blocks(sDO, kk, ATOM), idG,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 256, desc_k_atoms(sdSt, kk, ATOM), desc_mn_blocks(sQ, kk, ATOM), idG,
+                  (i > 0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit(&pd_done[pb]);
+      umma_commit(pd_done);
       umma_commit(&q_empty[qs]);
+      return true;
+    };
+    for (int i = 0; ok && i < n_rt; ++i) {
+      const int qs = i % QS;
+      // S^T(i) once dP^T(i - 1) has been copied out of the score buffer
+      if (!sync.wait(&q_full[qs], (i / QS) & 1)) { ok = false; break; }
+      if (i > 0 && !sync.wait(sc_free, 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 32768);
+      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 32768);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_tmem_a(tmem, tmem + 384 + kk * 8, desc_k_atoms(sQ, kk, ATOM), idS,
+                         kk > 0 ? 1u : 0u);
+      umma_commit(sc_full);
+      issued = true;
+      if (i > 0 && !issue_grads(i - 1)) { ok = false; break; }
+      // dP^T(i) once S^T(i) has been copied out
+      if (!sync.wait(sc_free, 0)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_tmem_a(tmem, tmem + 448 + kk * 8, desc_k_atoms(sDO, kk, ATOM), idS,
+                         kk > 0 ? 1u : 0u);
+      umma_commit(sc_full);
     }
+    if (ok && n_rt > 0 && !issue_grads(n_rt - 1)) ok = false;
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
       umma_commit(drain);
       mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
-    // Softmax warps: warp 4 + 4 half + quarter owns key rows 32 quarter ..
-    // 32 quarter + 31 (its TMEM lanes) and query columns 32 half .. 32 half + 31.
+    // ------------------------------------------------ softmax warps
+    // Warp 4 + 4 half + quarter owns key rows 32 quarter .. 32 quarter + 31
+    // (its TMEM lanes) and query columns 64 half .. 64 half + 63.
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
     const int krow = quarter * 32 + lane;  // key inside the tile
     const int key = j0 + krow;
+    const bool kvalid = key < T;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
+    // This thread's halves of the K and V rows into tensor memory.
+    const long krow_g = ((long)b * T + key) * HD + half * 64;
+    row64_to_tmem(tmem + lane_off + 384 + half * 32, kg + krow_g, kvalid);
+    row64_to_tmem(tmem + lane_off + 448 + half * 32, vg + krow_g, kvalid);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(kv_full);
     bool ok = true;
     for (int i = 0; i < n_rt; ++i) {
       const int st = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!sync.wait(&s_full[st], ph) || !sync.wait(&info_full[st], ph)) { ok = false; break; }
+      if (!sync.wait(sc_full, 0) || !sync.wait(&info_full[st], (i >> 1) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      float s[32], dp[32];
-      tmem_ld_32cols(tmem + lane_off + st * 64 + half * 32, s);
-      tmem_ld_32cols(tmem + lane_off + 128 + st * 64 + half * 32, dp);
+      float s[64], dp[64];
+      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(s));
+      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(s + 32));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-      const float* il = info_lse + st * 64 + half * 32;
-      const float* id = info_dl + st * 64 + half * 32;
-      const int* it = info_tok + st * 64 + half * 32;
-      // Rows are in token order, so it[0] is the smallest token of these 32
-      // rows; rows past the sequence carry token -1.  Only tiles that cross
-      // the diagonal (or the end) need the mask.
-      const bool need_mask = j0 + BKV - 1 > it[0] || it[31] < 0;
+      if (lane == 0) mbar_arrive(sc_free);
+      const float* il = info_lse + st * 128 + half * 64;
+      const float* id = info_dl + st * 128 + half * 64;
+      const int* it = info_tok + st * 128 + half * 64;
+      // Rows are in token order: it[0] is the smallest token of these 64
+      // rows; rows past the sequence carry token -1.
+      const bool need_mask = j0 + BKV - 1 > it[0] || it[63] < 0;
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
+      for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = reinterpret_cast<const float4*>(il)[c4];
-        const float4 d4 = reinterpret_cast<const float4*>(id)[c4];
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c4 * 4 + e;
           float p = ex2(fmaf(s[c], sl2, -lv[e]));
           if (need_mask && key > it[c]) p = 0.f;
           s[c] = p;
-          dp[c] = p * (dp[c] - dv4[e]);
+        }
+      }
+      if (!sync.wait(sc_full, 1)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sc_free);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 d4 = reinterpret_cast<const float4*>(id)[c4];
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c4 * 4 + e;
+          dp[c] = s[c] * (dp[c] - dv4[e]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&info_free[st]);
-      const int pb = i & 1;
-      if (i > 1) {  // dV/dK MMAs of tile i - 2 have read this P^T, dS^T buffer
-        if (!sync.wait(&pd_done[pb], ((i >> 1) - 1) & 1)) { ok = false; break; }
+      if (i > 0) {  // dV/dK MMAs of tile i - 1 have read P^T, dS^T
+        if (!sync.wait(pd_done, (i - 1) & 1)) { ok = false; break; }
       }
-      store_half_row_atom(smem + PT_OFF + pb * 16384, krow, half * 4, s);
-      store_half_row_atom(smem + DST_OFF + pb * 16384, krow, half * 4, dp);
+      store_row_atom(smem + PT_OFF + half * ATOM, krow, s);
+      store_row_atom(smem + DST_OFF + half * ATOM, krow, dp);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
+      if (lane == 0) mbar_arrive(p_full);
     }
-    // MMAs complete in issue order: the last tile's done means all are.
-    if (ok && n_rt > 0 && sync.wait(&pd_done[(n_rt - 1) & 1], ((n_rt - 1) >> 1) & 1)) {
+    if (ok && n_rt > 0 && sync.wait(pd_done, (n_rt - 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
-      const bool valid = key < T;
       const long tok = (long)b * T + key;
 #pragma unroll 1
       for (int c = 2 * half; c < 2 * half + 2; ++c) {
         float v[32];
+        tmem_ld_32cols(tmem + lane_off + 128 + c * 32, v);
+        if (kvalid) store_bf16_32(dv + tok * ldv + c * 32, v, 1.f);
         tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
-        if (valid) store_bf16_32(dv + tok * ldv + c * 32, v, 1.f);
-        tmem_ld_32cols(tmem + lane_off + 384 + c * 32, v);
-        if (valid) store_bf16_32(dk + tok * ldk + c * 32, v, scale);
+        if (kvalid) store_bf16_32(dk + tok * ldk + c * 32, v, scale);
       }
     }
   }
@@ -962,13 +977,12 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   note_launch(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ) ||
-      !map3(&mk, k, T, B, bkv::BKV) || !map3(&mv, v, T, B, bkv::BKV))
+  if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ))
     return cudaErrorInvalidValue;
   dim3 gk(B, (unsigned)((T + bkv::BKV - 1) / bkv::BKV));
-  attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(mq, mdo, mk, mv, lse, delta,
-                                                             (nc::bf16*)dk, ldk, (nc::bf16*)dv,
-                                                             ldv, T, H, ctx.err, ctx.timeout_ns);
+  attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(
+      mq, mdo, (const nc::bf16*)k, (const nc::bf16*)v, lse, delta, (nc::bf16*)dk, ldk,
+      (nc::bf16*)dv, ldv, T, H, ctx.err, ctx.timeout_ns);
   return launched(1);
 }
 

@@ -16,6 +16,7 @@ from .nanochat_step import (  # noqa: F401
     attention_bwd,
     backward,
     cross_entropy,
+    evaluate,
     forward,
     rmsnorm,
     rmsnorm_bwd,

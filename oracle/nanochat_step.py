@@ -195,6 +195,34 @@ def forward(shape, params: dict, ids: np.ndarray, targets: np.ndarray | None = N
     return cache
 
 
+def evaluate(shape, params: dict, ids: np.ndarray, targets: np.ndarray,
+             token_bytes: np.ndarray | None = None) -> tuple[float, float | None]:
+    """Forward-only evaluation: (mean next-token loss in nats over targets >= 0,
+    bits per byte or None).
+
+    Walkthrough, section "预训练": the run reports validation bits per byte,
+    the per-token loss normalised by the bytes each token stands for so that
+    it does not depend on the tokenizer.  `token_bytes[v]` is the byte length
+    of token v.  Reading: tokens of byte length 0 (special tokens) are left
+    out of both sums; bpb = sum(loss_t) / (ln 2 * sum(bytes(y_t))).
+    """
+    cache = forward(shape, params, ids)
+    s = cache["s"].reshape(-1, shape.vocab)
+    y = targets.reshape(-1)
+    rows = np.nonzero(y >= 0)[0]
+    m = np.max(s[rows], axis=-1, keepdims=True)
+    lse = (m + np.log(np.sum(np.exp(s[rows] - m), axis=-1, keepdims=True)))[:, 0]
+    nats = lse - s[rows, y[rows]]
+    loss = float(nats.sum() / max(rows.size, 1))
+    if token_bytes is None:
+        return loss, None
+    nb = np.asarray(token_bytes, dtype=np.int64)[y[rows]]
+    keep = nb > 0
+    total = int(nb[keep].sum())
+    bpb = float(nats[keep].sum() / (np.log(2.0) * total)) if total > 0 else float("nan")
+    return loss, bpb
+
+
 def backward(shape, params: dict, cache: dict) -> dict:
     """Hand-derived backward of `forward`; returns d(loss)/d(every weight)."""
     ids = cache["ids"]

@@ -328,3 +328,35 @@ def test_pages_depth20_arithmetic():
     total = flops.flops_per_token(s, g["tokens_per_row"], n_kv_head=s.n_head) * g["tokens_total_approx"]
     assert abs(total / g["flops_total_approx"] - 1) < 0.05
     assert abs(flops.n_params(s) / 502.0e6 - 1) < 0.001            # MQA, as built
+
+
+# ---------------------------------------------------------------- evaluation
+def test_eval_bpb_closed_form_zero_head():
+    """Zero LM head: every token's loss is ln V, so bpb = n ln V / (ln 2 sum
+    bytes) exactly; tokens of byte length 0 drop out of both sums."""
+    shape = nc_synth.TINY.shape
+    ids, tg = nc_synth.make_tokens(shape.vocab, 2, 16, seed=3, dist="uniform")
+    w = nc_synth.make_weights(shape, seed=1, bf16=False, zero=("w_lm",))
+    P = {k: v.astype(np.float64) for k, v in w.items()}
+    rng = np.random.default_rng(0)
+    nbytes = rng.integers(1, 7, size=shape.vocab)
+    nbytes[:5] = 0
+    loss, bpb = oracle.evaluate(shape, P, ids, tg, nbytes)
+    lnv = math.log(shape.vocab)
+    assert loss == pytest.approx(lnv, rel=1e-12)
+    y = tg.reshape(-1)
+    keep = nbytes[y] > 0
+    assert bpb == pytest.approx(keep.sum() * lnv / (math.log(2) * nbytes[y].sum()), rel=1e-12)
+
+
+def test_eval_loss_equals_training_loss_and_one_byte_tokens_give_bits_per_token():
+    shape = nc_synth.TINY.shape
+    ids, tg = nc_synth.make_tokens(shape.vocab, 2, 16, seed=4, dist="uniform")
+    tg[0, :3] = -1
+    w = nc_synth.make_weights(shape, seed=2, bf16=False)
+    P = {k: v.astype(np.float64) for k, v in w.items()}
+    loss, bpb = oracle.evaluate(shape, P, ids, tg, np.ones(shape.vocab, dtype=np.int64))
+    train = oracle.forward(shape, P, ids, tg)["loss"]
+    assert loss == pytest.approx(train, rel=1e-12)
+    assert bpb == pytest.approx(loss / math.log(2), rel=1e-12)
+    assert oracle.evaluate(shape, P, ids, tg)[1] is None

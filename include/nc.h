@@ -154,6 +154,19 @@ nc_status nc_step(const nc_config* cfg, int B, int T, const int32_t* ids,
 
 /* Synchronises `stream`, reads the device error word of `ws`, clears it and
  * returns NC_OK, NC_ERR_TIMEOUT or NC_ERR_TOKEN_RANGE (or NC_ERR_CUDA). */
+/* Forward-only evaluation (walkthrough, pretraining section: the run
+ * reports validation bits per byte -- the next-token loss normalised by the
+ * bytes per token, comparable across tokenizers).  Runs the forward pass and
+ * the loss without any backward; writes out[0] = mean loss over targets >= 0
+ * (nats) and out[1] = sum of the losses of targets whose byte length is > 0,
+ * divided by ln 2 times the sum of those byte lengths (bits per byte), or
+ * NaN when token_bytes is NULL.  token_bytes: int32 [vocab] byte length of
+ * each token id (0 for special tokens, which then count in neither sum).
+ * out: device float[2], 8-byte aligned.  Same workspace as nc_step. */
+nc_status nc_eval(const nc_config* cfg, int B, int T, const int32_t* ids, const int32_t* targets,
+                  const int32_t* token_bytes, const void* wte, const nc_layer_w* layers,
+                  const void* w_lm, float* out, void* ws, size_t ws_bytes, void* stream);
+
 nc_status nc_get_device_status(void* ws, void* stream);
 
 const char* nc_status_string(nc_status s);

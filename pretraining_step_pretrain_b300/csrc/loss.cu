@@ -139,6 +139,58 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   Vec4<float>::store(p + 4, *reinterpret_cast<const float(*)[4]>(v + 4));
 }
 
+// Forward-only evaluation: mean loss over valid targets and bits per byte
+// (fixed-order tree in one CTA).  out[0] = sum(loss_t) / n in nats;
+// out[1] = sum over targets with byte length > 0 of loss_t / (ln 2 * sum of
+// their byte lengths), or NaN without a byte table.
+__global__ void eval_loss_kernel(const float* __restrict__ lse, const float* __restrict__ s_tgt,
+                                 const int* __restrict__ targets,
+                                 const int* __restrict__ token_bytes, int M, int V,
+                                 float* out, int* err) {
+  __shared__ double sh_l[1024], sh_lb[1024];
+  __shared__ long long sh_n[1024], sh_b[1024];
+  double acc = 0.0, acc_b = 0.0;
+  long long cnt = 0, nbytes = 0;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) {
+    const int y = targets[i];
+    if (y >= 0 && y < V) {
+      const double nats = (double)lse[i] - (double)s_tgt[i];
+      acc += nats;
+      ++cnt;
+      if (token_bytes) {
+        const int nb = token_bytes[y];
+        if (nb > 0) {
+          acc_b += nats;
+          nbytes += nb;
+        }
+      }
+    } else if (y >= V || y < -1) {
+      raise_error(err, DEV_TOKEN_RANGE, 3, i);
+    }
+  }
+  sh_l[threadIdx.x] = acc;
+  sh_lb[threadIdx.x] = acc_b;
+  sh_n[threadIdx.x] = cnt;
+  sh_b[threadIdx.x] = nbytes;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) {
+      sh_l[threadIdx.x] += sh_l[threadIdx.x + s];
+      sh_lb[threadIdx.x] += sh_lb[threadIdx.x + s];
+      sh_n[threadIdx.x] += sh_n[threadIdx.x + s];
+      sh_b[threadIdx.x] += sh_b[threadIdx.x + s];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const long long n = sh_n[0] > 0 ? sh_n[0] : 1;
+    out[0] = (float)(sh_l[0] / (double)n);
+    out[1] = (token_bytes && sh_b[0] > 0)
+                 ? (float)(sh_lb[0] / (0.6931471805599453 * (double)sh_b[0]))
+                 : __int_as_float(0x7fc00000);
+  }
+}
+
 // dz in place.  TS: stored capped logit type, TG: gradient type written over
 // it (same size).  One CTA per row; 8 elements (16 B of fp16/bf16, two 16 B
 // vectors of fp32) per thread and step.
@@ -194,6 +246,13 @@ cudaError_t ce_rows_from_partials(const float* part, int n_part, float* lse, int
 cudaError_t ce_loss(const float* lse, const float* s_tgt, const int* targets, int M, int V,
                     float* loss, float* inv_n, const Ctx& ctx) {
   ce_loss_kernel<<<1, 1024, 0, ctx.stream>>>(lse, s_tgt, targets, M, V, loss, inv_n, ctx.err);
+  return launched(1);
+}
+
+cudaError_t eval_loss(const float* lse, const float* s_tgt, const int* targets,
+                      const int* token_bytes, int M, int V, float* out, const Ctx& ctx) {
+  eval_loss_kernel<<<1, 1024, 0, ctx.stream>>>(lse, s_tgt, targets, token_bytes, M, V, out,
+                                               ctx.err);
   return launched(1);
 }
 

@@ -275,9 +275,9 @@ nc_status block_fwd_impl(const nc_config& c, int layer, int B, int T, const nc_l
   return NC_OK;
 }
 
-nc_status lmhead_impl(const nc_config& c, int B, int T, const float* x_L, const void* w_lm,
-                      const int32_t* targets, float* loss, float* dx_L, float* dw_lm,
-                      int accumulate, void* ws, const Layout& L, const Ctx& ctx) {
+// Final norm, logits, softcap, per-row log-sum-exp and capped target logit.
+nc_status lm_fwd_impl(const nc_config& c, const float* x_L, const void* w_lm,
+                      const int32_t* targets, void* ws, const Layout& L, const Ctx& ctx) {
   const bool bf = c.dtype == NC_BF16;
   const int M = L.M, d = c.d_model, V = c.vocab;
   void* xf = at(ws, L.xf);
@@ -285,7 +285,6 @@ nc_status lmhead_impl(const nc_config& c, int B, int T, const float* x_L, const 
   void* logits = at(ws, L.big);
   float* lse = at<float>(ws, L.lse_row);
   float* s_tgt = at<float>(ws, L.s_tgt);
-  float* inv_n = at<float>(ws, L.loss_misc);
   NC_RUN("lm.norm", rmsnorm_fwd(bf, x_L, xf, rstdf, M, d, c.eps, ctx));
   if (bf) {
     GemmArgs g = gemm_args(GEMM_NT, EPI_SOFTCAP_CE, M, V, d, xf, d, w_lm, d, logits, V);
@@ -304,6 +303,24 @@ nc_status lmhead_impl(const nc_config& c, int B, int T, const float* x_L, const 
     NC_RUN("lm.softcap_rows", softcap_rows_f32(static_cast<float*>(logits), targets, lse, s_tgt, M, V, c.softcap,
                              ctx));
   }
+  return NC_OK;
+}
+
+nc_status lmhead_impl(const nc_config& c, int B, int T, const float* x_L, const void* w_lm,
+                      const int32_t* targets, float* loss, float* dx_L, float* dw_lm,
+                      int accumulate, void* ws, const Layout& L, const Ctx& ctx) {
+  const bool bf = c.dtype == NC_BF16;
+  const int M = L.M, d = c.d_model, V = c.vocab;
+  void* xf = at(ws, L.xf);
+  float* rstdf = at<float>(ws, L.rstdf);
+  void* logits = at(ws, L.big);
+  float* lse = at<float>(ws, L.lse_row);
+  float* s_tgt = at<float>(ws, L.s_tgt);
+  float* inv_n = at<float>(ws, L.loss_misc);
+  (void)B;
+  (void)T;
+  nc_status st = lm_fwd_impl(c, x_L, w_lm, targets, ws, L, ctx);
+  if (st != NC_OK) return st;
   NC_RUN("lm.loss", ce_loss(lse, s_tgt, targets, M, V, loss, inv_n, ctx));
   NC_RUN("lm.dlogits", ce_dlogits(bf, logits, lse, targets, inv_n, M, V, c.softcap, ctx));
   // dW_lm = G^T xf ; dxf = G W_lm
@@ -513,6 +530,34 @@ nc_status nc_step(const nc_config* cfg, int B, int T, const int32_t* ids, const 
         NC_OK)
       return s;
   return embed_bwd_impl(*cfg, B, T, ids, wte, dx, dwte, accumulate, ws, L, ctx);
+}
+
+nc_status nc_eval(const nc_config* cfg, int B, int T, const int32_t* ids, const int32_t* targets,
+                  const int32_t* token_bytes, const void* wte, const nc_layer_w* layers,
+                  const void* w_lm, float* out, void* ws, size_t ws_bytes, void* stream) {
+  Layout L;
+  nc_status s = check_ws(cfg, B, T, ws, ws_bytes, &L);
+  if (s == NC_OK) s = check_ptrs({ids, targets, wte, w_lm});
+  if (s != NC_OK) return s;
+  if (!layers) return fail(NC_ERR_INVALID_ARG, "layers array is null");
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return fail(NC_ERR_INVALID_ARG, "out pointer is null or not 8-byte aligned");
+  if (token_bytes && (reinterpret_cast<uintptr_t>(token_bytes) & 3u))
+    return fail(NC_ERR_INVALID_ARG, "token_bytes is misaligned");
+  for (int l = 0; l < cfg->depth; ++l) {
+    if ((s = check_ptrs({layers[l].w_qkv, layers[l].w_o, layers[l].w_fc, layers[l].w_proj})) !=
+        NC_OK)
+      return fail(s, "layer %d: %s", l, g_last_error.c_str());
+  }
+  const Ctx ctx = make_ctx(ws, stream);
+  float* x = at<float>(ws, L.x);
+  if ((s = embed_fwd_impl(*cfg, B, T, ids, wte, x, ws, L, ctx)) != NC_OK) return s;
+  for (int l = 0; l < cfg->depth; ++l)
+    if ((s = block_fwd_impl(*cfg, l, B, T, layers[l], x, ws, L, ctx)) != NC_OK) return s;
+  if ((s = lm_fwd_impl(*cfg, x, w_lm, targets, ws, L, ctx)) != NC_OK) return s;
+  NC_RUN("eval.loss", eval_loss(at<float>(ws, L.lse_row), at<float>(ws, L.s_tgt), targets,
+                                token_bytes, L.M, cfg->vocab, out, ctx));
+  return NC_OK;
 }
 
 nc_status nc_get_device_status(void* ws, void* stream) {

@@ -116,6 +116,8 @@ cudaError_t ce_rows_from_partials(const float* part, int n_part, float* lse, int
                                   const Ctx& ctx);
 cudaError_t ce_loss(const float* lse, const float* s_tgt, const int* targets, int M, int V,
                     float* loss, float* inv_n, const Ctx& ctx);
+cudaError_t eval_loss(const float* lse, const float* s_tgt, const int* targets,
+                      const int* token_bytes, int M, int V, float* out, const Ctx& ctx);
 cudaError_t ce_dlogits(bool bf16, void* s, const float* lse, const int* targets,
                        const float* inv_n, int M, int V, float cap, const Ctx& ctx);
 

@@ -29,7 +29,7 @@ EXPORTS = ("nc_workspace_bytes", "nc_embed_norm", "nc_block_fwd", "nc_lmhead_sof
            "nc_attention_bwd_noalloc",
            "nc_launch_count", "nc_profile_start", "nc_profile_stop", "nc_profile_record",
            "nc_selftest_wait_timeout", "nc_gemm_batched", "nc_optimizer_workspace_bytes",
-           "nc_optimizer_step")
+           "nc_optimizer_step", "nc_eval")
 
 
 class NcConfig(ctypes.Structure):
@@ -118,6 +118,7 @@ def lib() -> ctypes.CDLL:
                                     P, I, ctypes.c_long, P, ctypes.c_float, ctypes.c_float, P, S,
                                     P]),
             "nc_optimizer_workspace_bytes": (S, [C]),
+            "nc_eval": (I, [C, I, I, P, P, P, P, ctypes.POINTER(NcLayerW), P, P, P, S, P]),
             "nc_optimizer_step": (I, [C, ctypes.POINTER(NcOptConfig), I, ctypes.c_float, P, P,
                                       ctypes.POINTER(NcLayerF), P, P, ctypes.POINTER(NcLayerWC),
                                       P, P, ctypes.POINTER(NcLayerG), P, P, P, P,
@@ -340,6 +341,16 @@ class Step:
 
     def status(self) -> int:
         return get_device_status(self.ws)
+
+    def evaluate(self, ids, targets, token_bytes=None) -> torch.Tensor:
+        """Forward-only nc_eval on device ids/targets; returns the device
+        tensor [mean loss (nats), bits per byte (NaN without token_bytes)]."""
+        out = torch.zeros(2, dtype=torch.float32, device=self.device)
+        p, n = _ws(self.ws)
+        _check(lib().nc_eval(ctypes.byref(self.cfg), self.B, self.T, _ptr(ids), _ptr(targets),
+                             _ptr(token_bytes), self.w["wte"].data_ptr(), self.layers,
+                             self.w["w_lm"].data_ptr(), out.data_ptr(), p, n, _stream(self.device)))
+        return out
 
 
 # Muon's published defaults (momentum 0.95, the quintic Newton-Schulz

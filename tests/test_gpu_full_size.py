@@ -103,3 +103,37 @@ def test_d20_full_size_step_finite_deterministic(d20_full):
     for k in a[1]:
         assert np.all(np.isfinite(a[1][k])), k
         assert np.array_equal(a[1][k], b[1][k]), k
+
+
+D30 = nc_synth.D30
+
+
+def test_d30_widths_short_sequence_match_oracle():
+    """The next rung of the depth ladder (depth 30: 1920 channels, 15 heads,
+    f 7680, V 65536), one row of 128 tokens, every gradient against the oracle."""
+    shape = D30.shape
+    ids, tg, w = inputs(shape, 1, 128, "bf16")
+    ref_loss, ref_grads = run_oracle(shape, ids, tg, w)
+    loss, grads, status = run_cuda_step(shape, "bf16", ids, tg, w)
+    assert status == 0
+    assert_parity("bf16", ref_loss, ref_grads, loss, grads)
+
+
+def test_d30_gradient_accumulation_over_micro_batches():
+    """Two micro-batches accumulated into the same gradient buffers
+    (accumulate = 1 on the second) equal the oracle's sum of both batches'
+    gradients at the d30 widths."""
+    shape = D30.shape
+    ids, tg, w = inputs(shape, 2, 64, "bf16")
+    ref_a = run_oracle(shape, ids[:1], tg[:1], w)
+    ref_b = run_oracle(shape, ids[1:], tg[1:], w)
+    st = nc.Step(shape, "bf16", 1, 64, w)
+    st.run(torch.from_numpy(ids[:1].copy()).cuda(), torch.from_numpy(tg[:1].copy()).cuda())
+    st.run(torch.from_numpy(ids[1:].copy()).cuda(), torch.from_numpy(tg[1:].copy()).cuda(),
+           accumulate=True)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    for k in ref_a[1]:
+        ref = ref_a[1][k] + ref_b[1][k]
+        cos, rel = grad_metrics(ref, st.g[k].double().cpu().numpy())
+        assert cos > 0.999 and rel < 3e-2, (k, cos, rel)

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import nc_synth
+import oracle
 from pretraining_step_pretrain_b300 import build, nc
 from tests.helpers import assert_parity, inputs, run_cuda_step, run_oracle
 
@@ -108,3 +109,31 @@ def test_step_is_deterministic():
     assert a[0] == b[0]
     for k in a[1]:
         assert np.array_equal(a[1][k], b[1][k]), k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_eval_matches_oracle(dtype):
+    """nc_eval (forward only): mean loss and bits per byte against the oracle,
+    with a byte table that has zero-length (special) tokens; its loss equals
+    the training step's."""
+    shape = nc_synth.TINY.shape if dtype == "f32" else nc_synth.SMALL.shape
+    B, T = (2, 64) if dtype == "f32" else (4, 128)
+    ids, tg, w = inputs(shape, B, T, dtype)
+    tg[0, :4] = -1
+    rng = np.random.default_rng(9)
+    nbytes = rng.integers(1, 9, size=shape.vocab).astype(np.int32)
+    nbytes[:3] = 0
+    P = {k: v.astype(np.float64) for k, v in w.items()}
+    ref_loss, ref_bpb = oracle.evaluate(shape, P, ids, tg, nbytes)
+    st = nc.Step(shape, dtype, B, T, w)
+    ids_d, tg_d = torch.from_numpy(ids).cuda(), torch.from_numpy(tg).cuda()
+    out = st.evaluate(ids_d, tg_d, torch.from_numpy(nbytes).cuda()).cpu().numpy()
+    no_bytes = st.evaluate(ids_d, tg_d).cpu().numpy()
+    step_loss = float(st.run(ids_d, tg_d).item())
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    tol = 1e-5 if dtype == "f32" else 2e-3
+    assert abs(out[0] - ref_loss) <= tol * ref_loss, (out[0], ref_loss)
+    assert abs(out[1] - ref_bpb) <= tol * ref_bpb, (out[1], ref_bpb)
+    assert np.isnan(no_bytes[1]) and no_bytes[0] == out[0]
+    assert out[0] == pytest.approx(step_loss, rel=1e-6)

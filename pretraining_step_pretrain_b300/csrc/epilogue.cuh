@@ -140,13 +140,9 @@ template <typename TOut>
 struct EpiRelu2Bwd {
   static constexpr bool kRowReduce = false;
   using Out = TOut;
-  // The tensor-core epilogue loads this tile row's `a` slice before it waits
-  // for the accumulator, so the global-load latency overlaps the main loop.
-  static constexpr bool kPrefetch = true;
-  static constexpr int kPreCols = 128 / sizeof(TOut);  // one 128-byte chunk of a
-  struct Pre {
-    uint4 q[8];
-  };
+  // The tensor-core kernel brings this tile's `a` in by TMA, one 128-byte
+  // chunk per row at a time, ahead of the accumulator (compute_aux).
+  static constexpr bool kAuxTma = true;
   TOut* du;
   const TOut* a;
   long ld;
@@ -156,16 +152,11 @@ struct EpiRelu2Bwd {
     asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
     return 2.f * r;
   }
-  __device__ __forceinline__ void prefetch(int row, int col, int, Pre& p) const {
-    const uint4* src = reinterpret_cast<const uint4*>(a + (long)row * ld + col);
+  template <int W>
+  __device__ __forceinline__ float compute_aux(int, int, float (&v)[W], int,
+                                               const float (&av)[W]) const {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) p.q[i] = __ldg(src + i);
-  }
-  __device__ __forceinline__ float compute_pre(int, int, float (&v)[kPreCols], int,
-                                               const Pre& p) const {
-    const TOut* av = reinterpret_cast<const TOut*>(p.q);
-#pragma unroll
-    for (int i = 0; i < kPreCols; ++i) v[i] *= two_sqrt(to_f(av[i]));
+    for (int i = 0; i < W; ++i) v[i] *= two_sqrt(av[i]);
     return 0.f;
   }
   template <int W>
@@ -187,28 +178,18 @@ template <typename TOut>
 struct EpiAxpby {
   static constexpr bool kRowReduce = false;
   using Out = TOut;
-  static constexpr bool kPrefetch = true;
-  static constexpr int kPreCols = 128 / sizeof(TOut);
-  struct Pre {
-    uint4 q[8];
-  };
+  static constexpr bool kAuxTma = true;  // aux chunks come in by TMA (compute_aux)
   TOut* c;
   const TOut* aux;
   long ld;
   long aux_bstride;
   float alpha, beta;
   __device__ __forceinline__ bool reduce() const { return false; }
-  __device__ __forceinline__ void prefetch(int row, int col, int z, Pre& p) const {
-    const uint4* src =
-        reinterpret_cast<const uint4*>(aux + (long)z * aux_bstride + (long)row * ld + col);
+  template <int W>
+  __device__ __forceinline__ float compute_aux(int, int, float (&v)[W], int,
+                                               const float (&av)[W]) const {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) p.q[i] = __ldg(src + i);
-  }
-  __device__ __forceinline__ float compute_pre(int, int, float (&v)[kPreCols], int,
-                                               const Pre& p) const {
-    const TOut* av = reinterpret_cast<const TOut*>(p.q);
-#pragma unroll
-    for (int i = 0; i < kPreCols; ++i) v[i] = alpha * to_f(av[i]) + beta * v[i];
+    for (int i = 0; i < W; ++i) v[i] = alpha * av[i] + beta * v[i];
     return 0.f;
   }
   template <int W>

@@ -242,19 +242,27 @@ cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* ou
                    : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, tc::HALF_ROWS, nb, g.b_bstride));
   ok = ok && make_tmap_out<typename Epi::Out>(&tcm, out, g.N, g.M, ldo, zslabs * nb,
                                               nb > 1 ? g.c_bstride : 0);
+  // Auxiliary operand (same layout as C) for the epilogues that read one;
+  // the others get C's map, unused.
+  constexpr bool kAux = tc::HasAuxTma<Epi>::value;
+  CUtensorMap tax = tcm;
+  if (kAux)
+    ok = ok && make_tmap_out<typename Epi::Out>(&tax, const_cast<void*>(g.aux), g.N, g.M, ldo,
+                                                nb, nb > 1 ? g.c_bstride : 0);
   if (!ok) return cudaErrorInvalidValue;
   auto kern = tc::gemm_bf16_tc_kernel<A_MN, B_MN, Epi>;
+  constexpr int smem_bytes = tc::SmemPlan<kAux>::BYTES;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   // One CTA pair (a 2-CTA cluster) per unit, at most one CTA per SM.
   const int grid = 2 * std::max(1, std::min(p.sch.units, ctx.num_sms / 2));
-  kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, ctx.stream>>>(ta, tb, tcm, p.sch, g.M, g.N, epi,
-                                                             ctx.err, ctx.timeout_ns);
+  kern<<<grid, tc::NUM_THREADS, smem_bytes, ctx.stream>>>(ta, tb, tcm, tax, p.sch, g.M, g.N, epi,
+                                                          ctx.err, ctx.timeout_ns);
   return launched(1);
 }
 

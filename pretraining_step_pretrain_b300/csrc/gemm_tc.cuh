@@ -44,18 +44,25 @@ constexpr int BM = 256;              // output rows per CTA pair
 constexpr int BN = 256;              // output columns
 constexpr int BK = 64;
 constexpr int HALF_ROWS = 128;       // rows of the A and of the B tile each CTA loads
-constexpr int STAGES = 6;
 constexpr int A_BYTES = HALF_ROWS * BK * 2;  // 16 KB
 constexpr int B_BYTES = HALF_ROWS * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 256;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-// Epilogue staging: two 128-row x 128-byte chunks of the output tile.
+// Epilogue staging: two 128-row x 128-byte chunks of the output tile, and
+// for epilogues with an auxiliary operand (same layout as C) two more for
+// its chunks, loaded by TMA ahead of use; those run a 5-stage operand ring.
 constexpr int STAGE_OUT_BYTES = HALF_ROWS * 128;  // 16 KB
-constexpr int OUT_OFF = STAGES * STAGE_BYTES;
-constexpr int BAR_OFF = OUT_OFF + 2 * STAGE_OUT_BYTES;
-constexpr int SMEM_BYTES = BAR_OFF + 256 /*barriers*/ + 1024 /*align slack*/;
-static_assert(SMEM_BYTES <= 232448, "GEMM shared memory exceeds 227 KB");
+template <bool kAux>
+struct SmemPlan {
+  static constexpr int kStages = kAux ? 5 : 6;
+  static constexpr int OUT_OFF = kStages * STAGE_BYTES;
+  static constexpr int AUX_OFF = OUT_OFF + 2 * STAGE_OUT_BYTES;
+  static constexpr int BAR_OFF = AUX_OFF + (kAux ? 2 * STAGE_OUT_BYTES : 0);
+  static constexpr int BYTES = BAR_OFF + 256 /*barriers*/ + 1024 /*align slack*/;
+  static_assert(BYTES <= 232448, "GEMM shared memory exceeds 227 KB");
+};
+constexpr int STAGES_MAX = 6;
 // Swizzle-128B atom: 8 rows of 128 bytes.  An MN-major operand half-tile is
 // stored as 128/64 = 2 column blocks of 64 elements, each BK rows of 128 B.
 constexpr int MN_BLOCK_BYTES = BK * 128;  // 8 KB
@@ -106,24 +113,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-// Epilogues that declare kPrefetch load their per-row operand for the whole
-// tile before waiting for the accumulator.
+// Epilogues that declare kAuxTma read a second operand with C's layout
+// (ReLU^2 backward: the saved activation; AXPBY: the addend); the kernel
+// brings its chunks in by TMA ahead of use and passes them to compute_aux.
 template <class E, class = void>
-struct HasPrefetch {
+struct HasAuxTma {
   static constexpr bool value = false;
 };
 template <class E>
-struct HasPrefetch<E, std::void_t<decltype(E::kPrefetch)>> {
-  static constexpr bool value = E::kPrefetch;
-};
-struct NoPre {};
-template <class E, bool kPre>
-struct PreOf {
-  using type = NoPre;
-};
-template <class E>
-struct PreOf<E, true> {
-  using type = typename E::Pre;
+struct HasAuxTma<E, std::void_t<decltype(E::kAuxTma)>> {
+  static constexpr bool value = E::kAuxTma;
 };
 
 enum WaitSite : int {
@@ -162,18 +161,36 @@ __device__ __forceinline__ void stage_row(uint8_t* chunk, int r, const float (&v
   }
 }
 
+// Inverse of stage_row for a 16-bit type: the 64 values of row `r` of a
+// 128B-swizzled [128 rows][128 B] chunk written by TMA.
+template <typename T>
+__device__ __forceinline__ void unstage_row(const uint8_t* chunk, int r, float (&a)[64]) {
+  const uint8_t* base = chunk + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 w = *reinterpret_cast<const uint4*>(base + ((q ^ (r & 7)) << 4));
+    const T* e = reinterpret_cast<const T*>(&w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[q * 8 + i] = to_f(e[i]);
+  }
+}
+
 template <bool A_MN, bool B_MN, class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const Sched sch, const int M,
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmAux, const Sched sch, const int M,
                         const int N, const Epi epi, int* err, const long long timeout_ns) {
+  constexpr bool kAux = HasAuxTma<Epi>::value;
+  using Plan = SmemPlan<kAux>;
+  constexpr int STAGES = Plan::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Plan::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -181,6 +198,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_ok = abort_flag + 1;  // [4]: the epilogue warps' accumulator waits
+  uint64_t* aux_full = reinterpret_cast<uint64_t*>(smem + Plan::BAR_OFF + 192);  // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -198,6 +216,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&acc_empty[b], 8);  // used on the even CTA: 4 epilogue warps x 2 CTAs
     }
     mbar_init(drain, 1);
+    mbar_init(&aux_full[0], 1);
+    mbar_init(&aux_full[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -205,6 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
+    if (kAux) tma_prefetch_desc(&tmAux);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -337,6 +358,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&acc_empty[1]), 0);
     const bool reduce = epi.reduce();
     int acc = 0, chunk_no = 0;
+    int aux_no = 0;                   // auxiliary chunks consumed so far
+    uint32_t aux_uses[2] = {0, 0};    // loads consumed per auxiliary buffer
+    uint32_t aux_issued[2] = {0, 0};  // loads issued per auxiliary buffer (issuer)
     uint32_t acc_phase = 0;
     for (int u = pair; u < sch.units; u += npairs) {
       int mt, nt, split, batch, kb0, kb1;
@@ -344,16 +368,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int r_in = quarter * 32 + lane;
       const int row0 = mt * BM + (int)rank * HALF_ROWS;
       const int row = row0 + r_in;
-      constexpr bool kPre = HasPrefetch<Epi>::value;
-      using Pre = typename std::conditional<kPre, typename PreOf<Epi, kPre>::type, NoPre>::type;
-      Pre pre[kPre ? NCH : 1];
-      if constexpr (kPre) {
-        static_assert(!kPre || Epi::kPreCols == W, "prefetch chunk must match the staging chunk");
-        if (row < M) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            if (nt * BN + c * W < N) epi.prefetch(row, nt * BN + c * W, batch, pre[c]);
-        }
+      // Chunks of this tile that lie inside C (a prefix of the NCH chunks).
+      const int nvalid = row0 >= M ? 0 : min(NCH, (N - nt * BN + W - 1) / W);
+      const int aux_base = aux_no;    // chunk c of this tile uses buffer (aux_base + c) & 1
+      auto issue_aux = [&](int c) {
+        const int bsel = (aux_base + c) & 1;
+        ++aux_issued[bsel];
+        mbar_arrive_expect_tx(&aux_full[bsel], STAGE_OUT_BYTES);
+        tma_load_3d(smem + Plan::AUX_OFF + bsel * STAGE_OUT_BYTES, &tmAux, &aux_full[bsel],
+                    nt * BN + c * W, row0, batch);
+      };
+      if constexpr (kAux) {
+        // The first two auxiliary chunks load while the tile still accumulates.
+        if (issuer)
+          for (int c = 0; c < min(2, nvalid); ++c) issue_aux(c);
       }
       int ok = 1;
       if (lane == 0)
@@ -369,24 +397,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       float row_acc = 0.f;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
+#pragma unroll 1
+      for (int c = 0; c < nvalid; ++c) {
         const int col = nt * BN + c * W;
-        // Chunks wholly outside C are skipped by all four warps alike; only
-        // stored chunks take a staging buffer, so the newest pending store
-        // always reads the other buffer.
-        if (col >= N || row0 >= M) continue;
         float v[W];
 #pragma unroll
         for (int h = 0; h < W / 32; ++h)
           tmem_ld_32cols(taddr + c * W + h * 32, *reinterpret_cast<float(*)[32]>(v + h * 32));
-        if (row < M) {
-          if constexpr (kPre)
-            row_acc += epi.compute_pre(row, col, v, batch, pre[c]);
-          else
-            row_acc += epi.template compute<W>(row, col, v, batch);
+        if constexpr (kAux) {
+          const int bsel = aux_no & 1;
+          int aok = 1;
+          if (lane == 0)
+            aok = mbar_wait_bounded(&aux_full[bsel], aux_uses[bsel] & 1u, abort_flag, err,
+                                    SITE_EPI_ACC_FULL, timeout_ns);
+          aok = __shfl_sync(0xffffffffu, aok, 0);
+          if (aok) {
+            mbar_try_wait(smem_u32(&aux_full[bsel]), aux_uses[bsel] & 1u);  // acquire in every lane
+            float av[64];
+            unstage_row<Out>(smem + Plan::AUX_OFF + bsel * STAGE_OUT_BYTES, r_in, av);
+            if (row < M) row_acc += epi.template compute_aux<W>(row, col, v, batch, av);
+          }
+          ++aux_uses[bsel];
+          ++aux_no;
+        } else {
+          if (row < M) row_acc += epi.template compute<W>(row, col, v, batch);
         }
-        uint8_t* chunk = smem + OUT_OFF + (chunk_no & 1) * STAGE_OUT_BYTES;
+        uint8_t* chunk = smem + Plan::OUT_OFF + (chunk_no & 1) * STAGE_OUT_BYTES;
         ++chunk_no;
         if (issuer) bulk_wait_group_read<1>();  // the store issued from this buffer is done reading
         named_bar_sync<128>();
@@ -399,6 +435,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           else
             tma_store_3d(&tmC, chunk, col, row0, split);
           bulk_commit_group();
+          // Every thread is past its read of this chunk's auxiliary buffer:
+          // refill it with chunk c + 2.
+          if constexpr (kAux) {
+            if (c + 2 < nvalid) issue_aux(c + 2);
+          }
         }
       }
       if (Epi::kRowReduce && row < M) epi.row_end(row, nt * BN, row_acc);
@@ -410,7 +451,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
-    if (issuer) bulk_wait_group_all();
+    if (issuer) {
+      bulk_wait_group_all();
+      // After an abort: let auxiliary loads already issued land before exit.
+      if constexpr (kAux) {
+        int none = 0;
+        for (int b2 = 0; b2 < 2; ++b2)
+          for (; aux_uses[b2] < aux_issued[b2]; ++aux_uses[b2])
+            mbar_wait_bounded(&aux_full[b2], aux_uses[b2] & 1u, &none, err, SITE_DRAIN,
+                              timeout_ns / 8);
+      }
+    }
   }
 
   tc_fence_before();

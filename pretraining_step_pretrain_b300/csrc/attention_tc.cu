@@ -72,6 +72,17 @@ __device__ __forceinline__ void store_half_row_atom(uint8_t* atom, int row, int 
   }
 }
 
+// (x - d) * p on both halves of a packed fp32 pair: one instruction each for
+// the subtract and the multiply instead of two.
+__device__ __forceinline__ void sub_mul2(float& r0, float& r1, float x0, float x1, float d0,
+                                         float d1, float p0, float p1) {
+  asm("{\n\t.reg .b64 x, d, p, r;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 d, {%4, %5};\n\tmov.b64 p, {%6, %7};\n\t"
+      "sub.rn.f32x2 r, x, d;\n\tmul.rn.f32x2 r, r, p;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1), "f"(d0), "f"(d1), "f"(p0), "f"(p1));
+}
+
 // 2^x on the special-function unit (approximate, flushes denormals; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float r;
@@ -89,20 +100,6 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// 64 bf16 of one row (a 128-byte global slice) into this thread's TMEM lane
-// as 32 columns, element 2i in the low half of column i.
-__device__ __forceinline__ void row64_to_tmem(uint32_t taddr, const bf16* src, bool valid) {
-  float v[32];
-  uint4 q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    q[i] = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0u, 0u, 0u, 0u);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(q);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
-  tmem_st_32cols(taddr, v);
 }
 
 // Store 32 fp32 values as bf16 to global (64 contiguous bytes).
@@ -492,24 +489,29 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
+    // Kept lean (see the dK/dV pass): descriptors are built once and a k-step
+    // or ring stage only moves the start-address field.
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idQ = idesc_bf16_mn(false, true, BQ, HD);
-    const uint32_t sDS = smem_u32(smem + DS_OFF);
+    constexpr uint64_t kStage = 32768 >> 4;
+    const uint64_t dKk = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);    // K-major
+    const uint64_t dKm = sdesc_sw128(smem_u32(smem + K_OFF), ATOM, 1024);  // MN-major
+    const uint64_t dVk = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
+    const uint64_t dSk = sdesc_sw128(smem_u32(smem + DS_OFF), 16, 1024);
+    auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
+    auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
     bool ok = sync.wait(q_full, 0), issued = false;
-    // S(j) and dP(j) into the single TMEM buffer once tile j - 1's copies are out.
+    // S(j) and dP(j) into their TMEM buffers once tile j - 1's copies are out.
     auto issue_s = [&](int j) -> bool {
       const int ks = j % KVS;
       if (!sync.wait(&kv_full[ks], (j / KVS) & 1)) return false;
       if (j > 0 && !sync.wait(s_free, (j - 1) & 1)) return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + ks * 32768);
-      const uint32_t sV = smem_u32(smem + V_OFF + ks * 32768);
+      const uint64_t bk = dKk + ks * kStage, bv = dVk + ks * kStage;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
-        umma_bf16_tmem_a(tmem + 0, tmem + 384 + kk * 8, desc_k_atoms(sK, kk, ATOM), idS,
-                         kk > 0 ? 1u : 0u);
-        umma_bf16_tmem_a(tmem + 128, tmem + 448 + kk * 8, desc_k_atoms(sV, kk, ATOM), idS,
-                         kk > 0 ? 1u : 0u);
+        umma_bf16_tmem_a(tmem + 0, tmem + 384 + kk * 8, bk + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_bf16_tmem_a(tmem + 128, tmem + 448 + kk * 8, bv + koff(kk), idS, kk > 0 ? 1u : 0u);
       }
       umma_commit(s_full);
       issued = true;
@@ -520,11 +522,10 @@ __global__ void __launch_bounds__(NT, 1)
       const int ks = j % KVS, db = j & 1;
       if (!sync.wait(&ds_full[db], (j >> 1) & 1)) return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + ks * 32768);
+      const uint64_t a = dSk + db * kStage, bk = dKm + ks * kStage;
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, desc_k_atoms(sDS + db * 32768, kk, ATOM),
-                  desc_mn_blocks(sK, kk, ATOM), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 256, a + koff(kk), bk + moff(kk), idQ, (j > 0 || kk > 0) ? 1u : 0u);
       umma_commit(&dq_done[db]);
       umma_commit(&kv_empty[ks]);
       return true;
@@ -552,30 +553,47 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
     const long grow = (long)b * TH + r;
-    // delta = rowsum(dO * O): each half sums 64 of the 128 dims.
+    // delta = rowsum(dO * O): each half sums 64 of the 128 dims.  All three
+    // row slices (Q, dO, O) are requested before any is used, so the
+    // prologue pays one memory latency, not one per slice.
     float* dl_part = reinterpret_cast<float*>(smem + DL_OFF);
+    uint4 qa[8], da[8], oa[8];
     float dl = 0.f, lse2 = 0.f;
-    if (valid) {
-      const bf16* orow = o + grow * HD + half * 64;
-      const bf16* drow = dout + grow * HD + half * 64;
-#pragma unroll 4
-      for (int i = 0; i < 64; i += 8) {
-        const uint4 a = *reinterpret_cast<const uint4*>(orow + i);
-        const uint4 d = *reinterpret_cast<const uint4*>(drow + i);
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(q + grow * HD + half * 64);
+      const uint4* drow = reinterpret_cast<const uint4*>(dout + grow * HD + half * 64);
+      const uint4* orow = reinterpret_cast<const uint4*>(o + grow * HD + half * 64);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 fa = __bfloat1622float2(a2[k]), fd = __bfloat1622float2(d2[k]);
-          dl += fa.x * fd.x + fa.y * fd.y;
-        }
+      for (int i = 0; i < 8; ++i) {
+        qa[i] = valid ? qrow[i] : make_uint4(0u, 0u, 0u, 0u);
+        da[i] = valid ? drow[i] : make_uint4(0u, 0u, 0u, 0u);
+        oa[i] = valid ? orow[i] : make_uint4(0u, 0u, 0u, 0u);
       }
-      lse2 = lse[grow] * kLog2e;
+      if (valid) lse2 = lse[grow] * kLog2e;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&oa[i]);
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&da[i]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(a2[k]), fd = __bfloat1622float2(d2[k]);
+        dl += fa.x * fd.x + fa.y * fd.y;
+      }
     }
     // This thread's halves of the Q and dO rows into tensor memory (the A
     // operands of every S and dP MMA); rows past the sequence are zero.
-    row64_to_tmem(tmem + lane_off + 384 + half * 32, q + grow * HD + half * 64, valid);
-    row64_to_tmem(tmem + lane_off + 448 + half * 32, dout + grow * HD + half * 64, valid);
+    {
+      float v[32];
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(qa);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
+      tmem_st_32cols(tmem + lane_off + 384 + half * 32, v);
+      w = reinterpret_cast<const uint32_t*>(da);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
+      tmem_st_32cols(tmem + lane_off + 448 + half * 32, v);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(q_full);
@@ -603,11 +621,15 @@ __global__ void __launch_bounds__(NT, 1)
       const int key0 = j * BKV + half * 64;
       const bool need_mask = rows_ragged || key0 + 63 > t0;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float p = ex2(fmaf(s[i], sl2, -lse2));
-        if (need_mask && (!valid || key0 + i > t)) p = 0.f;
-        s[i] = p * (dp[i] - dl);
+      for (int i = 0; i < 64; ++i) s[i] = ex2(fmaf(s[i], sl2, -lse2));
+      if (need_mask) {  // key key0 + i is visible to token t; padding rows see nothing
+        const int lim = valid ? t - key0 : -1;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i > lim) s[i] = 0.f;
       }
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) sub_mul2(s[i], s[i + 1], dp[i], dp[i + 1], dl, dl, s[i], s[i + 1]);
       const int db = j & 1;
       if (j > 1) {  // the dQ MMA of tile j - 2 has read this dS buffer
         if (!sync.wait(&dq_done[db], ((j >> 1) - 1) & 1)) { ok = false; break; }
@@ -650,62 +672,108 @@ __global__ void __launch_bounds__(NT, 1)
 namespace bkv {
 constexpr int BKV = 128, BQ = 128;
 constexpr int ATOM = 16384;                   // [128 rows][64] bf16
-constexpr int QS = 2;                         // Q / dO ring stages (64 KB each)
-constexpr int Q_OFF = 0;                      // QS x 32 KB
-constexpr int DO_OFF = Q_OFF + QS * 32768;    // QS x 32 KB
-constexpr int PT_OFF = DO_OFF + QS * 32768;   // 32 KB ([128 keys][128 rows])
-constexpr int DST_OFF = PT_OFF + 32768;       // 32 KB
-constexpr int INFO_OFF = DST_OFF + 32768;     // [2][128] x (lse2, delta, tok)
-constexpr int BAR_OFF = INFO_OFF + 2 * 128 * 12 + 128;
-constexpr int SMEM = BAR_OFF + 256 + 1024;
-static_assert(SMEM <= 232448, "dK/dV pass shared memory exceeds 227 KB");
+constexpr int QS = 3;                         // Q ring stages (32 KB each)
+constexpr int DS = 2;                         // dO ring stages (32 KB each)
+constexpr int Q_OFF = 0;
+constexpr int DO_OFF = Q_OFF + QS * 32768;
+constexpr int K_OFF = DO_OFF + DS * 32768;    // 32 KB, the CTA's 128 keys
+constexpr int V_OFF = K_OFF + 32768;          // 32 KB
+constexpr int INFO_OFF = V_OFF + 32768;       // [2][128] x (lse2, delta)
+constexpr int BAR_OFF = INFO_OFF + 2 * 128 * 8;
+constexpr int USED = BAR_OFF + 256;
+constexpr int SMEM = 232448;                  // the per-CTA maximum
+constexpr int SLACK = SMEM - USED;            // room to align the base to 1024 bytes
+constexpr int kGroup = 8;                     // sequences per launch group (L2 residency)
+static_assert(SLACK >= 0, "dK/dV pass shared memory exceeds 227 KB");
 }  // namespace bkv
 
+// 32 bf16 pairs of this thread's row into its TMEM lane (32 columns).
+__device__ __forceinline__ void pairs_to_tmem(uint32_t taddr, const uint32_t (&p)[32]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
+  tmem_st_32cols(taddr, v);
+}
+
+// dK/dV pass: one CTA per 128-key tile, K and V resident in shared memory,
+// query tiles (Q, dO) streamed through two TMA rings.  Per query tile i the
+// MMA thread issues, in this order,
+//   S^T(i) = K Q(i)^T,  dV += P^T(i-1) dO(i-1),  dP^T(i) = V dO(i)^T,
+//   dK += dS^T(i-1) Q(i-1),
+// so the tensor pipe always has the previous tile's gradient products to run
+// while the softmax warps turn S^T(i) into P^T(i) and dP^T(i) into dS^T(i).
+// S^T and dP^T share one 128-column score buffer; the softmax warps write
+// P^T and dS^T as bf16 into tensor memory, where the dV and dK products read
+// them as their A operand.  Shared-memory traffic per query tile is then the
+// TMA fills (64 KB) and the B operands plus K, V (192 KB): below the tensor
+// pipe's time for the four 128 x 128 x 128 products.
 __global__ void __launch_bounds__(NT, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                            const __grid_constant__ CUtensorMap tmDO, const bf16* __restrict__ kg,
-                            const bf16* __restrict__ vg, const float* __restrict__ lse,
+                            const __grid_constant__ CUtensorMap tmDO,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const float* __restrict__ lse,
                             const float* __restrict__ delta, bf16* __restrict__ dk, long ldk,
                             bf16* __restrict__ dv, long ldv, int T, int H, int* err,
                             long long timeout_ns) {
   using namespace bkv;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > (uint32_t)SLACK) {  // uniform: no barrier or tensor memory touched yet
+    if (threadIdx.x == 0) raise_error(err, DEV_CUDA, SITE_ATTN, (int)pad);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* kv_full = bars + 0;             // K, V in tensor memory (softmax warps)
-  uint64_t* q_full = bars + 1;              // [QS]
-  uint64_t* q_empty = bars + 1 + QS;        // [QS]
-  uint64_t* sc_full = bars + 1 + 2 * QS;    // score buffer holds S^T, then dP^T
-  uint64_t* sc_free = bars + 2 + 2 * QS;    // copied out, one arrival per softmax warp
-  uint64_t* p_full = bars + 3 + 2 * QS;     // P^T, dS^T stored, one arrival per softmax warp
-  uint64_t* pd_done = bars + 4 + 2 * QS;    // dV, dK MMAs of the tile done
-  uint64_t* drain = bars + 5 + 2 * QS;
-  uint64_t* info_full = bars + 6 + 2 * QS;  // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 8 + 2 * QS;  // [2], one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * QS);
+  uint64_t* kv_full = bars + 0;      // K, V tiles landed (TMA)
+  uint64_t* q_full = bars + 1;       // [QS]
+  uint64_t* q_empty = bars + 4;      // [QS]
+  uint64_t* do_full = bars + 7;      // [DS]
+  uint64_t* do_empty = bars + 9;     // [DS]
+  uint64_t* sc_full = bars + 11;     // score buffer holds S^T, then dP^T
+  uint64_t* sc_free = bars + 12;     // copied out, one arrival per softmax warp
+  uint64_t* p_full = bars + 13;      // P^T stored, one arrival per softmax warp
+  uint64_t* ds_full = bars + 14;     // dS^T stored, one arrival per softmax warp
+  uint64_t* pt_free = bars + 15;     // dV MMAs done reading P^T (and every earlier MMA)
+  uint64_t* dst_free = bars + 16;    // dK MMAs done reading dS^T (and every earlier MMA)
+  uint64_t* drain = bars + 17;
+  uint64_t* info_full = bars + 18;   // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 20;   // [2], one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);        // [2][128]
-  float* info_dl = info_lse + 2 * 128;                                // [2][128]
-  int* info_tok = reinterpret_cast<int*>(info_dl + 2 * 128);          // [2][128]
+  float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);  // [2][128]
+  float* info_dl = info_lse + 2 * 128;                          // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
-  const int j0 = blockIdx.y * BKV;  // heaviest (earliest keys) first
+  // Launch order: sequences in groups of kGroup; inside a group the heaviest
+  // key tiles (the earliest keys, which meet every later query row) first,
+  // sequence fastest.  The Q and dO rows that a group streams stay resident
+  // in L2 while its CTAs run, and heavy tiles still start first.
+  const int NY = (T + BKV - 1) / BKV;
+  const int g0 = (int)(blockIdx.x / (kGroup * NY)) * kGroup;  // first sequence of the group
+  const int gsz = min(kGroup, (int)(gridDim.x / NY) - g0);
+  const int r = (int)blockIdx.x - g0 * NY;
+  const int b = g0 + r % gsz;
+  const int j0 = (r / gsz) * BKV;
   const long TH = (long)T * H;
   const long rt0 = ((long)j0 * H) / BQ;
   const int n_rt = (int)((TH + BQ - 1) / BQ - rt0);
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, NSW);
+    mbar_init(kv_full, 1);
     for (int i = 0; i < QS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
+    for (int i = 0; i < DS; ++i) {
+      mbar_init(&do_full[i], 1);
+      mbar_init(&do_empty[i], 1);
+    }
     mbar_init(sc_full, 1);
     mbar_init(sc_free, NSW);
     mbar_init(p_full, NSW);
-    mbar_init(pd_done, 1);
+    mbar_init(ds_full, NSW);
+    mbar_init(pt_free, 1);
+    mbar_init(dst_free, 1);
     mbar_init(drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&info_full[i], 32);
@@ -723,7 +791,8 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const CtaSync sync{abort_flag, err, timeout_ns};
-  // TMEM columns: score at 0, dV at 128, dK at 256, K at 384, V at 448 (bf16 pairs).
+  // TMEM columns: score at 0, dV at 128, dK at 256, P^T at 384, dS^T at 448
+  // (bf16 pairs: query rows 2c, 2c + 1 in column c).
 
   if (warp == 3) {
     // ------------------------------------------------ per-row data of each query tile
@@ -736,84 +805,120 @@ __global__ void __launch_bounds__(NT, 1)
         const bool v = rr < TH;
         info_lse[st * 128 + c] = v ? lse[(long)b * TH + rr] * kLog2e : 0.f;
         info_dl[st * 128 + c] = v ? delta[(long)b * TH + rr] : 0.f;
-        info_tok[st * 128 + c] = v ? (int)(rr / H) : -1;
       }
       mbar_arrive(&info_full[st]);
     }
   }
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer (Q, dO)
-    int armed[QS];
-    for (int i = 0; i < QS; ++i) armed[i] = -1;
+    // ------------------------------------------------ TMA producer (K, V; Q ring, dO ring)
+    mbar_arrive_expect_tx(kv_full, 4 * ATOM);
+    tma_load_3d(smem + K_OFF, &tmK, kv_full, 0, j0, b);
+    tma_load_3d(smem + K_OFF + ATOM, &tmK, kv_full, 64, j0, b);
+    tma_load_3d(smem + V_OFF, &tmV, kv_full, 0, j0, b);
+    tma_load_3d(smem + V_OFF + ATOM, &tmV, kv_full, 64, j0, b);
+    int armed_q[QS], armed_do[DS];
+    for (int i = 0; i < QS; ++i) armed_q[i] = -1;
+    for (int i = 0; i < DS; ++i) armed_do[i] = -1;
     for (int i = 0; i < n_rt; ++i) {
-      const int qs = i % QS;
-      const uint32_t qph = (i / QS) & 1;
       const int rr = (int)((rt0 + i) * BQ);
+      const int qs = i % QS, ds = i % DS;
+      const uint32_t qph = (i / QS) & 1, dph = (i / DS) & 1;
       if (!sync.wait(&q_empty[qs], qph ^ 1u)) break;
-      mbar_arrive_expect_tx(&q_full[qs], 4 * ATOM);
+      mbar_arrive_expect_tx(&q_full[qs], 2 * ATOM);
       tma_load_3d(smem + Q_OFF + qs * 32768, &tmQ, &q_full[qs], 0, rr, b);
       tma_load_3d(smem + Q_OFF + qs * 32768 + ATOM, &tmQ, &q_full[qs], 64, rr, b);
-      tma_load_3d(smem + DO_OFF + qs * 32768, &tmDO, &q_full[qs], 0, rr, b);
-      tma_load_3d(smem + DO_OFF + qs * 32768 + ATOM, &tmDO, &q_full[qs], 64, rr, b);
-      armed[qs] = (int)qph;
+      armed_q[qs] = (int)qph;
+      if (!sync.wait(&do_empty[ds], dph ^ 1u)) break;
+      mbar_arrive_expect_tx(&do_full[ds], 2 * ATOM);
+      tma_load_3d(smem + DO_OFF + ds * 32768, &tmDO, &do_full[ds], 0, rr, b);
+      tma_load_3d(smem + DO_OFF + ds * 32768 + ATOM, &tmDO, &do_full[ds], 64, rr, b);
+      armed_do[ds] = (int)dph;
     }
     if (*abort_flag) {
       int none = 0;
+      mbar_wait_bounded(kv_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
       for (int i = 0; i < QS; ++i)
-        if (armed[i] >= 0)
-          mbar_wait_bounded(&q_full[i], (uint32_t)armed[i], &none, err, SITE_ATTN,
+        if (armed_q[i] >= 0)
+          mbar_wait_bounded(&q_full[i], (uint32_t)armed_q[i], &none, err, SITE_ATTN,
+                            timeout_ns / 8);
+      for (int i = 0; i < DS; ++i)
+        if (armed_do[i] >= 0)
+          mbar_wait_bounded(&do_full[i], (uint32_t)armed_do[i], &none, err, SITE_ATTN,
                             timeout_ns / 8);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
-    // Per query tile i: S^T(i); dV, dK of tile i - 1; dP^T(i).
+    // Kept lean: this thread shares its scheduler with two softmax warps, and
+    // every instruction between two MMA groups is time the tensor pipe can
+    // run dry.  Descriptors are built once; a k-step or a ring stage only
+    // moves the 14-bit start-address field (shared memory < 256 KB: no carry).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
     constexpr uint32_t idG = idesc_bf16_mn(false, true, BKV, HD);
-    const uint32_t sPt = smem_u32(smem + PT_OFF), sdSt = smem_u32(smem + DST_OFF);
+    constexpr uint64_t kStage = 32768 >> 4;
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
+    const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);    // K-major
+    const uint64_t dQm = sdesc_sw128(smem_u32(smem + Q_OFF), ATOM, 1024);  // MN-major
+    const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
+    const uint64_t dOm = sdesc_sw128(smem_u32(smem + DO_OFF), ATOM, 1024);
+    // start-field offsets of k-step kk: K-major across 64-wide atoms, MN-major by 16 rows
+    auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
+    auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
     bool ok = sync.wait(kv_full, 0), issued = false;
-    auto issue_grads = [&](int i) -> bool {  // dV += P^T dO, dK += dS^T Q of tile i
-      const int qs = i % QS;
-      if (!sync.wait(p_full, i & 1)) return false;
-      tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 32768);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 32768);
+    int qs = 0, ds = 0, pqs = 0, pds = 0;  // ring stages of tiles i and i - 1
+    uint32_t qph = 0, dph = 0;
+    for (int i = 0; ok && i <= n_rt; ++i) {
+      const bool cur = i < n_rt, prev = i > 0;
+      if (cur) {  // S^T(i) once dP^T(i - 1) has been copied out of the score buffer
+        if (!sync.wait(&q_full[qs], qph) || (prev && !sync.wait(sc_free, 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t bq = dQk + qs * kStage;
 #pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk) {
-        umma_bf16(tmem + 128, desc_k_atoms(sPt, kk, ATOM), desc_mn_blocks(sDO, kk, ATOM), idG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(tmem + 256, desc_k_atoms(sdSt, kk, ATOM), desc_mn_blocks(sQ, kk, ATOM), idG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem, dK + koff(kk), bq + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_commit(sc_full);
+        issued = true;
       }
-      umma_commit(pd_done);
-      umma_commit(&q_empty[qs]);
-      return true;
-    };
-    for (int i = 0; ok && i < n_rt; ++i) {
-      const int qs = i % QS;
-      // S^T(i) once dP^T(i - 1) has been copied out of the score buffer
-      if (!sync.wait(&q_full[qs], (i / QS) & 1)) { ok = false; break; }
-      if (i > 0 && !sync.wait(sc_free, 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + Q_OFF + qs * 32768);
-      const uint32_t sDO = smem_u32(smem + DO_OFF + qs * 32768);
+      if (prev) {  // dV += P^T dO of tile i - 1
+        if (!sync.wait(p_full, (i - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bo = dOm + pds * kStage;
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16_tmem_a(tmem, tmem + 384 + kk * 8, desc_k_atoms(sQ, kk, ATOM), idS,
-                         kk > 0 ? 1u : 0u);
-      umma_commit(sc_full);
-      issued = true;
-      if (i > 0 && !issue_grads(i - 1)) { ok = false; break; }
-      // dP^T(i) once S^T(i) has been copied out
-      if (!sync.wait(sc_free, 0)) { ok = false; break; }
-      tc_fence_after();
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          umma_bf16_tmem_a(tmem + 128, tmem + 384 + kk * 8, bo + moff(kk), idG,
+                           (i > 1 || kk > 0) ? 1u : 0u);
+        umma_commit(pt_free);
+        umma_commit(&do_empty[pds]);
+      }
+      if (cur) {  // dP^T(i) once S^T(i) has been copied out
+        if (!sync.wait(&do_full[ds], dph) || !sync.wait(sc_free, 0)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bo = dOk + ds * kStage;
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16_tmem_a(tmem, tmem + 448 + kk * 8, desc_k_atoms(sDO, kk, ATOM), idS,
-                         kk > 0 ? 1u : 0u);
-      umma_commit(sc_full);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem, dV + koff(kk), bo + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_commit(sc_full);
+      }
+      if (prev) {  // dK += dS^T Q of tile i - 1
+        if (!sync.wait(ds_full, (i - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bq = dQm + pqs * kStage;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          umma_bf16_tmem_a(tmem + 256, tmem + 448 + kk * 8, bq + moff(kk), idG,
+                           (i > 1 || kk > 0) ? 1u : 0u);
+        umma_commit(dst_free);
+        umma_commit(&q_empty[pqs]);
+      }
+      pqs = qs;
+      pds = ds;
+      if (++qs == QS) { qs = 0; qph ^= 1u; }
+      if (++ds == DS) { ds = 0; dph ^= 1u; }
     }
-    if (ok && n_rt > 0 && !issue_grads(n_rt - 1)) ok = false;
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
       umma_commit(drain);
@@ -830,75 +935,80 @@ __global__ void __launch_bounds__(NT, 1)
     const bool kvalid = key < T;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
-    // This thread's halves of the K and V rows into tensor memory.
-    const long krow_g = ((long)b * T + key) * HD + half * 64;
-    row64_to_tmem(tmem + lane_off + 384 + half * 32, kg + krow_g, kvalid);
-    row64_to_tmem(tmem + lane_off + 448 + half * 32, vg + krow_g, kvalid);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(kv_full);
     bool ok = true;
     for (int i = 0; i < n_rt; ++i) {
       const int st = i & 1;
+      // packed rows rowbase .. rowbase + 63 are this thread's query columns
+      const long rowbase = (rt0 + i) * BQ + half * 64;
       if (!sync.wait(sc_full, 0) || !sync.wait(&info_full[st], (i >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[64], dp[64];
-      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(s));
-      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+      float x[64];
+      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(x));
+      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sc_free);
       const float* il = info_lse + st * 128 + half * 64;
-      const float* id = info_dl + st * 128 + half * 64;
-      const int* it = info_tok + st * 128 + half * 64;
-      // Rows are in token order: it[0] is the smallest token of these 64
-      // rows; rows past the sequence carry token -1.
-      const bool need_mask = j0 + BKV - 1 > it[0] || it[63] < 0;
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = reinterpret_cast<const float4*>(il)[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c4 * 4 + e;
-          float p = ex2(fmaf(s[c], sl2, -lv[e]));
-          if (need_mask && key > it[c]) p = 0.f;
-          s[c] = p;
-        }
+        x[c4 * 4 + 0] = ex2(fmaf(x[c4 * 4 + 0], sl2, -l4.x));
+        x[c4 * 4 + 1] = ex2(fmaf(x[c4 * 4 + 1], sl2, -l4.y));
+        x[c4 * 4 + 2] = ex2(fmaf(x[c4 * 4 + 2], sl2, -l4.z));
+        x[c4 * 4 + 3] = ex2(fmaf(x[c4 * 4 + 3], sl2, -l4.w));
       }
-      if (!sync.wait(sc_full, 1)) { ok = false; break; }
+      // Row rr (token rr / H) sees this key iff rr >= key * H; rows at or past
+      // T H are padding.  Warp-uniform test: only tiles on the diagonal or at
+      // the end of the sequence mask anything.
+      if (rowbase < (long)(j0 + BKV - 1) * H || rowbase + 64 > TH) {
+        const long lo = (long)key * H - rowbase, hi = TH - rowbase;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < lo || c >= hi) x[c] = 0.f;
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pk[j] = pack2(x[2 * j], x[2 * j + 1]);
+      if (i > 0 && !sync.wait(pt_free, (i - 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(dp));
-      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sc_free);
-#pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 d4 = reinterpret_cast<const float4*>(id)[c4];
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c4 * 4 + e;
-          dp[c] = s[c] * (dp[c] - dv4[e]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&info_free[st]);
-      if (i > 0) {  // dV/dK MMAs of tile i - 1 have read P^T, dS^T
-        if (!sync.wait(pd_done, (i - 1) & 1)) { ok = false; break; }
-      }
-      store_row_atom(smem + PT_OFF + half * ATOM, krow, s);
-      store_row_atom(smem + DST_OFF + half * ATOM, krow, dp);
-      fence_proxy_async_smem();
+      pairs_to_tmem(tmem + lane_off + 384 + half * 32, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      // dS^T = P^T (dP^T - delta), with P^T as stored (bf16)
+      if (!sync.wait(sc_full, 1)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(x));
+      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sc_free);
+      const float* id = info_dl + st * 128 + half * 64;
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 d4 = reinterpret_cast<const float4*>(id)[c4];
+        const uint32_t p01 = pk[c4 * 2], p23 = pk[c4 * 2 + 1];
+        float a0, a1, a2, a3;
+        sub_mul2(a0, a1, x[c4 * 4 + 0], x[c4 * 4 + 1], d4.x, d4.y, __uint_as_float(p01 << 16),
+                 __uint_as_float(p01 & 0xffff0000u));
+        sub_mul2(a2, a3, x[c4 * 4 + 2], x[c4 * 4 + 3], d4.z, d4.w, __uint_as_float(p23 << 16),
+                 __uint_as_float(p23 & 0xffff0000u));
+        pk[c4 * 2] = pack2(a0, a1);
+        pk[c4 * 2 + 1] = pack2(a2, a3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&info_free[st]);
+      if (i > 0 && !sync.wait(dst_free, (i - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      pairs_to_tmem(tmem + lane_off + 448 + half * 32, pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
     }
-    if (ok && n_rt > 0 && sync.wait(pd_done, (n_rt - 1) & 1)) {
+    if (ok && n_rt > 0 && sync.wait(dst_free, (n_rt - 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       const long tok = (long)b * T + key;
@@ -979,9 +1089,10 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   if (e != cudaSuccess) return e;
   if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ))
     return cudaErrorInvalidValue;
-  dim3 gk(B, (unsigned)((T + bkv::BKV - 1) / bkv::BKV));
+  static_assert(bkv::BKV == bdq::BKV, "the dK/dV pass reuses the K, V maps of the dQ pass");
+  const unsigned gk = (unsigned)B * (unsigned)((T + bkv::BKV - 1) / bkv::BKV);
   attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(
-      mq, mdo, (const nc::bf16*)k, (const nc::bf16*)v, lse, delta, (nc::bf16*)dk, ldk,
+      mq, mdo, mk, mv, lse, delta, (nc::bf16*)dk, ldk,
       (nc::bf16*)dv, ldv, T, H, ctx.err, ctx.timeout_ns);
   return launched(1);
 }

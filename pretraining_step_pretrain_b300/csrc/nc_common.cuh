@@ -15,7 +15,9 @@ typedef __nv_bfloat16 bf16;
 //   word[0] status (nc_status value; first writer wins)
 //   word[1] site code of the first error (which kernel / wait)
 //   word[2] detail (offending token index, ...)
-enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_TOKEN_RANGE = 6 };
+//   DEV_CUDA: a kernel found its launch unusable (e.g. a dynamic shared
+//   memory base it cannot align) and did nothing.
+enum DevErr : int { DEV_OK = 0, DEV_CUDA = 4, DEV_TIMEOUT = 5, DEV_TOKEN_RANGE = 6 };
 
 // A null word (a caller with no workspace) records nothing; the kernel still
 // stops the work that failed.
@@ -137,14 +139,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives up
 // (returns false) when *abort_flag is set by another role of the CTA, or after
 // timeout_ns, in which case it records DEV_TIMEOUT with `site` and sets
-// *abort_flag so the other roles stop too.
+// *abort_flag so the other roles stop too.  A nonzero sleep_ns sleeps between
+// polls: for roles off the critical path, so that their polling does not take
+// issue slots from the warps sharing their scheduler.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort_flag, int* err, int site,
-                                                  long long timeout_ns) {
+                                                  long long timeout_ns, unsigned sleep_ns = 0) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(addr, parity)) return true;
     if ((i & 15u) == 0) {
       if (*abort_flag) return false;

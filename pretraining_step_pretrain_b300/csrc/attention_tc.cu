@@ -394,26 +394,52 @@ __global__ void __launch_bounds__(NT, 1)
 // ~60% of the tensor rate: their shared-memory operand traffic per FLOP is
 // higher).
 // ======================================================================
+// delta[r] = sum_d O[r][d] dO[r][d] in fp32 for every packed row r (the
+// softmax-gradient row term of the attention backward): 16 threads per row,
+// one 16-byte slice each, then a 16-lane shuffle sum.
+__global__ void __launch_bounds__(256)
+    attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
+                      float* __restrict__ delta, long rows) {
+  const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int part = threadIdx.x & 15;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * HD)[part];
+    const uint4 d = reinterpret_cast<const uint4*>(dout + row * HD)[part];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]), fd = __bfloat1622float2(d2[k]);
+      acc = fmaf(fa.x, fd.x, acc);
+      acc = fmaf(fa.y, fd.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) delta[row] = acc;
+}
+
 namespace bdq {
 constexpr int BQ = 128, BKV = 128;
 constexpr int ATOM = 16384;                  // [128 rows][64] bf16
 constexpr int KVS = 2;                       // K/V ring stages (64 KB each)
 constexpr int K_OFF = 0;                     // KVS x 32 KB ([128 keys][128 dims] = 2 atoms)
 constexpr int V_OFF = K_OFF + KVS * 32768;   // KVS x 32 KB
-constexpr int DS_OFF = V_OFF + KVS * 32768;  // 2 x 32 KB ([128 rows][128 keys], by tile parity)
-constexpr int DL_OFF = DS_OFF + 2 * 32768;   // [2][128] fp32 halves of delta
-constexpr int BAR_OFF = DL_OFF + 1024;
+constexpr int DS_OFF = V_OFF + KVS * 32768;  // 2 x 32 KB ([128 rows][128 keys], by tile parity);
+                                             // first the staging of the Q and dO tiles
+constexpr int BAR_OFF = DS_OFF + 2 * 32768;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 static_assert(SMEM <= 232448, "dQ pass shared memory exceeds 227 KB");
 }  // namespace bdq
 
 __global__ void __launch_bounds__(NT, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
-                          const bf16* __restrict__ o,
-                          const bf16* __restrict__ dout, const float* __restrict__ lse,
-                          bf16* __restrict__ dq, long ldq, float* __restrict__ delta, int T, int H,
-                          int* err, long long timeout_ns) {
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmDO, const float* __restrict__ lse,
+                          const float* __restrict__ delta, bf16* __restrict__ dq, long ldq, int T,
+                          int H, int* err, long long timeout_ns) {
   using namespace bdq;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -427,7 +453,8 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* ds_full = bars + 3 + 2 * KVS;   // [2] by tile parity, one arrival per softmax warp
   uint64_t* dq_done = bars + 5 + 2 * KVS;   // [2] by tile parity
   uint64_t* drain = bars + 7 + 2 * KVS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * KVS);
+  uint64_t* qd_full = bars + 8 + 2 * KVS;   // Q and dO tiles staged (TMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9 + 2 * KVS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -451,6 +478,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&dq_done[i], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(qd_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -466,7 +494,12 @@ __global__ void __launch_bounds__(NT, 1)
   // TMEM columns: S at 0, dP at 128, dQ at 256, Q at 384, dO at 448 (bf16 pairs).
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer (K, V)
+    // ------------------------------------------------ TMA producer (Q, dO; K, V)
+    mbar_arrive_expect_tx(qd_full, 4 * ATOM);
+    tma_load_3d(smem + DS_OFF, &tmQ, qd_full, 0, (int)r0, b);
+    tma_load_3d(smem + DS_OFF + ATOM, &tmQ, qd_full, 64, (int)r0, b);
+    tma_load_3d(smem + DS_OFF + 32768, &tmDO, qd_full, 0, (int)r0, b);
+    tma_load_3d(smem + DS_OFF + 32768 + ATOM, &tmDO, qd_full, 64, (int)r0, b);
     int armed[KVS];
     for (int i = 0; i < KVS; ++i) armed[i] = -1;
     for (int j = 0; j < nkv; ++j) {
@@ -482,6 +515,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (*abort_flag) {
       int none = 0;
+      mbar_wait_bounded(qd_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
       for (int i = 0; i < KVS; ++i)
         if (armed[i] >= 0)
           mbar_wait_bounded(&kv_full[i], (uint32_t)armed[i], &none, err, SITE_ATTN,
@@ -553,60 +587,36 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
     const long grow = (long)b * TH + r;
-    // delta = rowsum(dO * O): each half sums 64 of the 128 dims.  All three
-    // row slices (Q, dO, O) are requested before any is used, so the
-    // prologue pays one memory latency, not one per slice.
-    float* dl_part = reinterpret_cast<float*>(smem + DL_OFF);
-    uint4 qa[8], da[8], oa[8];
-    float dl = 0.f, lse2 = 0.f;
-    {
-      const uint4* qrow = reinterpret_cast<const uint4*>(q + grow * HD + half * 64);
-      const uint4* drow = reinterpret_cast<const uint4*>(dout + grow * HD + half * 64);
-      const uint4* orow = reinterpret_cast<const uint4*>(o + grow * HD + half * 64);
+    // This thread's halves of the Q and dO rows, staged by TMA in swizzled
+    // [128 rows][64] atoms, into tensor memory (the A operands of every S and
+    // dP MMA); rows past the sequence were filled with zeros.
+    const float dl = valid ? delta[grow] : 0.f;
+    const float lse2 = valid ? lse[grow] * kLog2e : 0.f;
+    bool ok = sync.wait(qd_full, 0);
+    if (ok) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        qa[i] = valid ? qrow[i] : make_uint4(0u, 0u, 0u, 0u);
-        da[i] = valid ? drow[i] : make_uint4(0u, 0u, 0u, 0u);
-        oa[i] = valid ? orow[i] : make_uint4(0u, 0u, 0u, 0u);
+      for (int m = 0; m < 2; ++m) {
+        const uint8_t* src = smem + DS_OFF + m * 32768 + half * ATOM + row * 128;
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+          v[c * 4 + 0] = __uint_as_float(w.x);
+          v[c * 4 + 1] = __uint_as_float(w.y);
+          v[c * 4 + 2] = __uint_as_float(w.z);
+          v[c * 4 + 3] = __uint_as_float(w.w);
+        }
+        tmem_st_32cols(tmem + lane_off + 384 + m * 64 + half * 32, v);
       }
-      if (valid) lse2 = lse[grow] * kLog2e;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&oa[i]);
-      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&da[i]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 fa = __bfloat1622float2(a2[k]), fd = __bfloat1622float2(d2[k]);
-        dl += fa.x * fd.x + fa.y * fd.y;
-      }
-    }
-    // This thread's halves of the Q and dO rows into tensor memory (the A
-    // operands of every S and dP MMA); rows past the sequence are zero.
-    {
-      float v[32];
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(qa);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
-      tmem_st_32cols(tmem + lane_off + 384 + half * 32, v);
-      w = reinterpret_cast<const uint32_t*>(da);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(w[i]);
-      tmem_st_32cols(tmem + lane_off + 448 + half * 32, v);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_full);
-    dl_part[half * 128 + row] = dl;
-    asm volatile("bar.sync 1, %0;" ::"n"(NSW * 32) : "memory");  // the 8 softmax warps
-    dl = dl_part[row] + dl_part[128 + row];
-    if (valid && half == 0) delta[grow] = dl;
     // Rows of this CTA hold tokens t0 .. t_last; a key tile needs the mask
     // only where it reaches past t0 (or the tile has rows past the sequence).
     const int t0 = (int)(r0 / H);
     const bool rows_ragged = r0 + BQ > TH;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
+    for (int j = 0; ok && j < nkv; ++j) {
       if (!sync.wait(s_full, j & 1)) { ok = false; break; }
       tc_fence_after();
       float s[64], dp[64];
@@ -1078,18 +1088,22 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   }
   const long TH = (long)T * H;
   CUtensorMap mq, mdo, mk, mv;
-  if (!map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV))
+  static_assert(bkv::BKV == bdq::BKV && bkv::BQ == bdq::BQ, "both passes share their maps");
+  if (!map3(&mk, k, T, B, bdq::BKV) || !map3(&mv, v, T, B, bdq::BKV) ||
+      !map3(&mq, q, TH, B, bdq::BQ) || !map3(&mdo, dout, TH, B, bdq::BQ))
     return cudaErrorInvalidValue;
-  dim3 gq(B, (unsigned)((TH + bdq::BQ - 1) / bdq::BQ));
-  attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
-      mk, mv, (const nc::bf16*)q, (const nc::bf16*)o, (const nc::bf16*)dout, lse, (nc::bf16*)dq,
-      ldq, delta, T, H, ctx.err, ctx.timeout_ns);
+  const long rows = (long)B * TH;
+  attn_delta_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, ctx.stream>>>(
+      (const nc::bf16*)o, (const nc::bf16*)dout, delta, rows);
   note_launch(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!map3(&mq, q, TH, B, bkv::BQ) || !map3(&mdo, dout, TH, B, bkv::BQ))
-    return cudaErrorInvalidValue;
-  static_assert(bkv::BKV == bdq::BKV, "the dK/dV pass reuses the K, V maps of the dQ pass");
+  dim3 gq(B, (unsigned)((TH + bdq::BQ - 1) / bdq::BQ));
+  attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
+      mk, mv, mq, mdo, lse, delta, (nc::bf16*)dq, ldq, T, H, ctx.err, ctx.timeout_ns);
+  note_launch(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const unsigned gk = (unsigned)B * (unsigned)((T + bkv::BKV - 1) / bkv::BKV);
   attn_bwd_dkdv_tc_kernel<<<gk, NT, bkv::SMEM, ctx.stream>>>(
       mq, mdo, mk, mv, lse, delta, (nc::bf16*)dk, ldk,

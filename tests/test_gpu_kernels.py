@@ -178,6 +178,12 @@ def test_attention_fwd_bwd_matches_oracle(dtype, h, B, T, H):
     np.testing.assert_allclose(lse.double().cpu().numpy(), lse_ref,
                                atol=2e-2 if dtype == "bf16" else 1e-5)
     for name in ref:
+        if not np.any(ref[name]):
+            # One visible key (T = 1): P = 1 and dP = delta, so dS and dq are
+            # exactly zero; the GPU's two fp32 reductions (the dP MMA and the
+            # delta row sum) leave only rounding-level residue.
+            assert np.abs(got[name]).max() < 1e-3, (name, np.abs(got[name]).max())
+            continue
         cos, rel = grad_metrics(ref[name], got[name])
         if dtype == "bf16":
             assert cos > 0.999 and rel < 2e-2, (name, cos, rel)

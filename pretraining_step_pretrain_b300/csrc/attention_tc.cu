@@ -115,6 +115,26 @@ __device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32], f
   }
 }
 
+// 32 bf16 pairs of this thread's row into its TMEM lane (32 columns).
+__device__ __forceinline__ void pairs_to_tmem(uint32_t taddr, const uint32_t (&p)[32]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
+  tmem_st_32cols(taddr, v);
+}
+
+// 16 bf16 pairs of this thread's row into its TMEM lane (16 columns).
+__device__ __forceinline__ void pairs16_to_tmem(uint32_t taddr, const uint32_t (&p)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]),
+      "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]),
+      "r"(p[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 struct CtaSync {
   volatile int* abort_flag;
   int* err;
@@ -129,18 +149,21 @@ struct CtaSync {
 // ======================================================================
 namespace fwd {
 constexpr int BQ = 128, BKV = 128;
+constexpr int NG = 4;                       // softmax column groups (4 warps each)
+constexpr int CW = BKV / NG;                // key columns per softmax thread
+constexpr int NSWF = 4 * NG;                // softmax warps (warps 4 .. 4 + NSWF - 1)
+constexpr int NTF = 32 * (4 + NSWF);        // threads per CTA
 constexpr int ATOM = 16384;                 // [128 rows][64] bf16
 constexpr int Q_OFF = 0;                    // 32 KB
 constexpr int K_OFF = 32768;                // 2 x 32 KB
 constexpr int V_OFF = K_OFF + 2 * 32768;    // 2 x 32 KB
-constexpr int P_OFF = V_OFF + 2 * 32768;    // 32 KB
-constexpr int RED_OFF = P_OFF + 32768;      // [2 parity][2 half][128] row maxima
-constexpr int LSUM_OFF = RED_OFF + 2048;    // [2 half][128] row sums
-constexpr int BAR_OFF = LSUM_OFF + 1024;
+constexpr int RED_OFF = V_OFF + 2 * 32768;  // [2 parity][NG][128] row maxima
+constexpr int LSUM_OFF = RED_OFF + 2 * NG * 128 * 4;  // [NG][128] row sums
+constexpr int BAR_OFF = LSUM_OFF + NG * 128 * 4;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 }  // namespace fwd
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(fwd::NTF, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ o,
@@ -157,12 +180,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* v_empty = bars + 7;  // [2]
   uint64_t* s_full = bars + 9;   // [2]
   uint64_t* s_free = bars + 11;  // [2], one arrival per softmax warp
-  uint64_t* p_full = bars + 13;  // one arrival per softmax warp
-  uint64_t* o_done = bars + 14;
-  uint64_t* drain = bars + 15;
-  uint64_t* red_full = bars + 16;  // [2], one arrival per softmax warp
-  uint64_t* lsum_full = bars + 18; // one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* p_full = bars + 13;   // [2] by P buffer, one arrival per softmax warp
+  uint64_t* pv_done = bars + 15;  // [2] by P buffer: the PV MMA that read it is done
+  uint64_t* drain = bars + 17;
+  uint64_t* red_full = bars + 18;  // [2], one arrival per softmax warp
+  uint64_t* lsum_full = bars + 20; // one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,14 +204,14 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSW);
+      mbar_init(&s_free[i], NSWF);
+      mbar_init(&p_full[i], NSWF);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, NSW);
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&red_full[0], NSW);
-    mbar_init(&red_full[1], NSW);
-    mbar_init(lsum_full, NSW);
+    mbar_init(&red_full[0], NSWF);
+    mbar_init(&red_full[1], NSWF);
+    mbar_init(lsum_full, NSWF);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -231,21 +254,26 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
+    // Descriptors are built once; a k-step or ring stage only moves the
+    // 14-bit start-address field (shared memory < 256 KB: no carry).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idPV = idesc_bf16_mn(false, true, BQ, HD);
-    const uint32_t sQ = smem_u32(smem + Q_OFF);
-    const uint32_t sP = smem_u32(smem + P_OFF);
+    constexpr uint64_t kStage = 32768 >> 4;
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), ATOM, 1024);  // MN-major
+    auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
+    auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
     bool ok = sync.wait(q_full, 0), issued = false;
     auto issue_s = [&](int j) -> bool {
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!sync.wait(&k_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + K_OFF + st * 32768);
+      const uint64_t bk = dK + st * kStage;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + st * BKV, desc_k_atoms(sQ, kk, ATOM), desc_k_atoms(sK, kk, ATOM), idS,
-                  kk > 0 ? 1u : 0u);
+        umma_bf16(tmem + st * BKV, dQ + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
       umma_commit(&s_full[st]);
       umma_commit(&k_empty[st]);
       issued = true;
@@ -254,16 +282,17 @@ __global__ void __launch_bounds__(NT, 1)
     if (ok) ok = issue_s(0);
     for (int j = 0; ok && j < nkv; ++j) {
       if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+      // O += P(j) V(j), P(j) read from tensor memory
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(p_full, j & 1) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
+      if (!sync.wait(&p_full[st], ph) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sV = smem_u32(smem + V_OFF + st * 32768);
+      const uint64_t bv = dV + st * kStage;
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, desc_k_atoms(sP, kk, ATOM), desc_mn_blocks(sV, kk, ATOM), idPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(o_done);
+        umma_bf16_tmem_a(tmem + 256, tmem + 384 + st * 64 + kk * 8, bv + moff(kk), idPV,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&pv_done[st]);
       umma_commit(&v_empty[st]);
     }
     if ((!ok || *abort_flag) && issued) {
@@ -273,11 +302,12 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax / epilogue
-    // Warp 4 + 4 half + quarter owns packed rows 32 quarter .. 32 quarter + 31
-    // (its TMEM lanes) and key columns 64 half .. 64 half + 63 of each tile;
-    // the two halves of a row exchange their maxima through shared memory.
+    // Warp 4 + 4 g + quarter owns packed rows 32 quarter .. 32 quarter + 31
+    // (its TMEM lanes) and key columns CW g .. CW g + CW - 1 of each tile; the
+    // NG column groups of a row exchange their maxima through shared memory.
+    // Four warps per scheduler hide each other's TMEM, barrier and SFU latency.
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int g = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
     const long r = r0 + row;
     const bool valid = r < TH;
@@ -287,52 +317,54 @@ __global__ void __launch_bounds__(NT, 1)
     float* red = reinterpret_cast<float*>(smem + RED_OFF);
     float* lsum = reinterpret_cast<float*>(smem + LSUM_OFF);
     const int t0 = (int)(r0 / H);
-    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's columns only
+    const int tmax = min(t, T - 1);  // the last key this row sees
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this group's columns only
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
       tc_fence_after();
-      float s[64];
-      tmem_ld_32cols(tmem + lane_off + st * BKV + half * 64, *reinterpret_cast<float(*)[32]>(s));
-      tmem_ld_32cols(tmem + lane_off + st * BKV + half * 64 + 32,
-                     *reinterpret_cast<float(*)[32]>(s + 32));
+      float s[CW];
+      tmem_ld_32cols(tmem + lane_off + st * BKV + g * CW, s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[st]);
-      const int key0 = j * BKV + half * 64;
-      // Keys past every row's token (or past the sequence) occur only in
-      // tiles reaching beyond t0, the first row's token.
-      const bool need_mask = key0 + 63 > t0;
+      const int key0 = j * BKV + g * CW;
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float x = s[i] * sl2;
-        if (need_mask && (key0 + i > t || key0 + i >= T)) x = -INFINITY;
-        s[i] = x;
-        mx = fmaxf(mx, x);
+      for (int i = 0; i < CW; ++i) {
+        s[i] *= sl2;
+        mx = fmaxf(mx, s[i]);
       }
-      // Exchange the halves' maxima (buffers alternate by tile parity, so a
+      // Keys past a row's token (or past the sequence) occur only in tiles
+      // reaching beyond t0, the first row's token.
+      if (key0 + CW - 1 > t0) {
+        const int lim = tmax - key0;
+        mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          if (i > lim) s[i] = -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
+      }
+      // Exchange the groups' maxima (buffers alternate by tile parity, so a
       // fast warp never overwrites values a slow one has yet to read).
-      float* rp = red + (j & 1) * 256;
-      rp[half * 128 + row] = mx;
+      float* rp = red + (j & 1) * NG * 128;
+      rp[g * 128 + row] = mx;
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[j & 1]);
       if (!sync.wait(&red_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
-      mx = fmaxf(rp[row], rp[128 + row]);
-      // PV of the previous tile must be done before O is rescaled and before
-      // the single P buffer is overwritten.
-      if (j > 0) {
-        if (!sync.wait(o_done, (j - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
+#pragma unroll
+      for (int q = 0; q < NG; ++q) mx = fmaxf(mx, rp[q * 128 + row]);
       if (mx > m_run + 8.f) {
         const float alpha = ex2(m_run - mx);  // 0 on the first tile
-        if (j > 0) {
+        if (j > 0) {  // O is rescaled once the PV MMA of the previous tile is done
+          if (!sync.wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t oc = tmem + lane_off + 256 + half * 64 + c * 32;
+          for (int c = g * CW; c < (g + 1) * CW; c += 32) {
+            const uint32_t oc = tmem + lane_off + 256 + c;
             float v[32];
             tmem_ld_32cols(oc, v);
 #pragma unroll
@@ -344,35 +376,42 @@ __global__ void __launch_bounds__(NT, 1)
         m_run = mx;
       }
       float ls = 0.f;
+      uint32_t pk[CW / 2];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p = ex2(s[i] - m_run);
-        s[i] = p;
-        ls += p;
+      for (int i = 0; i < CW; i += 2) {
+        const float p0 = ex2(s[i] - m_run), p1 = ex2(s[i + 1] - m_run);
+        ls += p0 + p1;
+        pk[i / 2] = pack2(p0, p1);
       }
       l_run += ls;
-      store_row_atom(smem + P_OFF + half * ATOM, row, s);
-      fence_proxy_async_smem();
+      // P(j) as bf16 pairs into P buffer st once the PV MMA of tile j - 2 has read it
+      if (j >= 2) {
+        if (!sync.wait(&pv_done[st], ((j - 2) >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+      }
+      pairs16_to_tmem(tmem + lane_off + 384 + st * 64 + g * (CW / 2), pk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    lsum[half * 128 + row] = l_run;
+    lsum[g * 128 + row] = l_run;
     __syncwarp();
     if (lane == 0) mbar_arrive(lsum_full);
     if (ok) ok = sync.wait(lsum_full, 0);
-    const float l_tot = lsum[row] + lsum[128 + row];
-    if (ok && sync.wait(o_done, (nkv - 1) & 1)) {
+    float l_tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < NG; ++q) l_tot += lsum[q * 128 + row];
+    if (ok && sync.wait(&pv_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1)) {
       tc_fence_after();
       const float inv = 1.f / l_tot;
       bf16* orow = o + ((long)b * TH + r) * HD;
 #pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+      for (int c = g * CW; c < (g + 1) * CW; c += 32) {
         float v[32];
-        tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
-        if (valid) store_bf16_32(orow + c * 32, v, inv);
+        tmem_ld_32cols(tmem + lane_off + 256 + c, v);
+        if (valid) store_bf16_32(orow + c, v, inv);
       }
-      if (valid && half == 0) lse[(long)b * TH + r] = (m_run + log2f(l_tot)) * kLn2;
+      if (valid && g == 0) lse[(long)b * TH + r] = (m_run + log2f(l_tot)) * kLn2;
     }
   }
   tc_fence_before();
@@ -696,14 +735,6 @@ constexpr int SLACK = SMEM - USED;            // room to align the base to 1024 
 constexpr int kGroup = 8;                     // sequences per launch group (L2 residency)
 static_assert(SLACK >= 0, "dK/dV pass shared memory exceeds 227 KB");
 }  // namespace bkv
-
-// 32 bf16 pairs of this thread's row into its TMEM lane (32 columns).
-__device__ __forceinline__ void pairs_to_tmem(uint32_t taddr, const uint32_t (&p)[32]) {
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
-  tmem_st_32cols(taddr, v);
-}
 
 // dK/dV pass: one CTA per 128-key tile, K and V resident in shared memory,
 // query tiles (Q, dO) streamed through two TMA rings.  Per query tile i the
@@ -1070,7 +1101,7 @@ cudaError_t attention_fwd_tc(int B, int T, int H, const void* q, const void* k, 
       !map3(&mv, v, T, B, fwd::BKV))
     return cudaErrorInvalidValue;
   dim3 grid(B, (unsigned)((TH + fwd::BQ - 1) / fwd::BQ));
-  attn_fwd_tc_kernel<<<grid, NT, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, T, H,
+  attn_fwd_tc_kernel<<<grid, fwd::NTF, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, T, H,
                                                           ctx.err, ctx.timeout_ns);
   return launched(1);
 }

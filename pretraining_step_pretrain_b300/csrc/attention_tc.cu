@@ -8,17 +8,20 @@
 // packed rows meets a single K/V tile and every K/V byte brought on chip
 // serves all H heads; key j is visible to packed row r iff j <= r / H.
 //
-// Every kernel is warp-specialised (384 threads): warp 0 issues TMA, warp 1
-// issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..11 are two
+// Every kernel is warp-specialised: warp 0 issues TMA, warp 1 issues
+// tcgen05.mma, warp 2 owns the TMEM allocation, and the warps from 4 on are
 // softmax warpgroups -- a thread owns one TMEM lane, i.e. one row of the
-// score tile, and half of its columns (the other half belongs to the thread
-// of the same lane in the other warpgroup), so row reductions need no
-// shuffles and two warps per scheduler hide each other's latency.  Probabilities go from
-// registers to 128B-swizzled shared memory as the next MMA's operand.  A
-// 64-wide [row][64 dims] swizzled tile is both a K-major operand (rows = N)
-// and an MN-major one (rows = K), so no operand is ever transposed.  All
-// mbarrier waits are bounded; on timeout the CTA records DEV_TIMEOUT, stops,
-// drains in-flight copies and MMAs, and frees TMEM.
+// score tile, and a slice of its columns (the slices of a row belong to the
+// threads of the same lane in the other warpgroups): two warpgroups of 64
+// columns in the backward passes (384 threads), four of 32 in the forward
+// (640 threads, four warps per scheduler).  Row reductions need no shuffles.
+// The probability-like operands (P in the forward, P^T and dS^T in the dK/dV
+// pass) go from registers to tensor memory as bf16 pairs and feed the next
+// MMA as its A operand; dS of the dQ pass goes to 128B-swizzled shared
+// memory.  A 64-wide [row][64 dims] swizzled tile is both a K-major operand
+// (rows = N) and an MN-major one (rows = K), so no operand is ever
+// transposed.  All mbarrier waits are bounded; on timeout the CTA records
+// DEV_TIMEOUT, stops, drains in-flight copies and MMAs, and frees TMEM.
 #include <algorithm>
 
 #include "nc_common.cuh"
@@ -31,8 +34,8 @@ namespace {
 using namespace tc;
 
 constexpr int HD = 128;
-constexpr int NT = 384;  // threads per CTA: 4 control warps + 2 softmax warpgroups
-constexpr int NSW = 8;   // softmax warps (warps 4..11); warp w reads TMEM lanes 32 (w % 4) ..
+constexpr int NT = 384;  // backward passes: 4 control warps + 2 softmax warpgroups
+constexpr int NSW = 8;   // their softmax warps (4..11); warp w reads TMEM lanes 32 (w % 4) ..
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int SITE_ATTN = 300;
@@ -53,22 +56,6 @@ __device__ __forceinline__ void store_row_atom(uint8_t* atom, int row, const flo
     q.z = pack2(x[ch * 8 + 4], x[ch * 8 + 5]);
     q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
     *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = q;
-  }
-}
-
-// Store 32 bf16 values (one half of a 64-wide row) into a [rows][64]
-// 128B-swizzled atom: 16-byte chunks chunk0 .. chunk0 + 3 of the row.
-__device__ __forceinline__ void store_half_row_atom(uint8_t* atom, int row, int chunk0,
-                                                    const float* x) {
-  uint8_t* base = atom + row * 128;
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    uint4 q;
-    q.x = pack2(x[ch * 8 + 0], x[ch * 8 + 1]);
-    q.y = pack2(x[ch * 8 + 2], x[ch * 8 + 3]);
-    q.z = pack2(x[ch * 8 + 4], x[ch * 8 + 5]);
-    q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
-    *reinterpret_cast<uint4*>(base + (((chunk0 + ch) ^ (row & 7)) << 4)) = q;
   }
 }
 

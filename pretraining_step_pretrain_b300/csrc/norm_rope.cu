@@ -7,6 +7,8 @@
 // RMSNorm (launch article, architecture list: RMSNorm carries no learnable
 // gain): y = x * r, r = 1/sqrt(mean(x^2) + eps).
 // Backward (from y = x r(x)): dx = r (dy - y * mean(dy * y)).
+#include <algorithm>
+
 #include "nc_common.cuh"
 #include "nc_internal.h"
 
@@ -268,7 +270,152 @@ __global__ void qknorm_rope_bwd_kernel(A* __restrict__ dqkv, const A* __restrict
   }
 }
 
+// ---- QK-norm + RoPE backward, staged: each warp streams whole tokens (the
+// gradient rows and the saved q, k rows) through a ring of kStages
+// shared-memory slots filled by bulk copies (one mbarrier per slot), so every
+// warp keeps kStages - 1 tokens of loads in flight without holding them in
+// registers.  Same arithmetic as qknorm_rope_bwd_kernel, which remains the
+// path for shapes whose slots do not fit in shared memory.  (The same
+// staging of the forward measured no faster than its register version.)
+constexpr int kStages = 3;
+constexpr int kStagedWarps = 4;
+constexpr int SITE_QKNORM = 400;
+
+// Order this thread's generic-proxy shared-memory reads before a later bulk
+// copy (async proxy) into the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Elements lane*E .. lane*E + E - 1 of a head row held in shared memory.
+template <typename A, int E>
+__device__ __forceinline__ void load_vec_s(const uint8_t* p, float (&x)[E]) {
+  load_vec<A, E>(reinterpret_cast<const A*>(p), x);
+}
+
+// A warp-private ring: slot s of warp w at sm + (w * kStages + s) * slot_bytes.
+struct WarpRing {
+  uint8_t* base;
+  uint64_t* bars;  // [kStages]
+  uint32_t slot_bytes;
+  __device__ uint8_t* slot(int s) const { return base + (size_t)s * slot_bytes; }
+};
+
+// On a timed-out wait: wait (bounded) for this warp's other copies in flight,
+// then the caller returns.
+__device__ __forceinline__ void ring_drain(const WarpRing& r, const int (&armed)[kStages],
+                                           int* err, long long timeout_ns) {
+  int none = 0;
+  for (int s = 0; s < kStages; ++s)
+    if (armed[s] >= 0)
+      mbar_wait_bounded(&r.bars[s], (uint32_t)armed[s], &none, err, SITE_QKNORM, timeout_ns / 8);
+}
+
+template <typename A, int E>
+__global__ void __launch_bounds__(32 * kStagedWarps)
+    qknorm_rope_bwd_staged_kernel(A* __restrict__ dqkv, const A* __restrict__ q,
+                                  const A* __restrict__ k, const float* __restrict__ rstd_qk,
+                                  const float2* __restrict__ tab, int M, int T, int H, int* err,
+                                  long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ uint64_t bars[kStagedWarps][kStages];
+  constexpr int h = 32 * E, half = h / 2;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nh = H + 1;  // query heads + the key head (the value gradient passes through)
+  const uint32_t row = (uint32_t)h * sizeof(A);
+  // slot: g (nh rows of the gradient) then z (H rows of q, one of k)
+  const WarpRing r{sm + (size_t)w * kStages * 2 * nh * row, bars[w], 2 * nh * row};
+  const long stride = (long)gridDim.x * kStagedWarps;
+  const long m0 = (long)blockIdx.x * kStagedWarps + w;
+  auto fill = [&](long m, int s) {
+    uint8_t* d = r.slot(s);
+    mbar_arrive_expect_tx(&r.bars[s], r.slot_bytes);
+    bulk_g2s(d, dqkv + m * (H + 2) * h, nh * row, &r.bars[s]);
+    bulk_g2s(d + nh * row, q + m * H * h, H * row, &r.bars[s]);
+    bulk_g2s(d + (2 * nh - 1) * row, k + m * h, row, &r.bars[s]);
+  };
+  int armed[kStages];
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&r.bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  for (int s = 0; s < kStages; ++s) {
+    const long m = m0 + s * stride;
+    armed[s] = m < M ? 0 : -1;
+    if (lane == 0 && m < M) fill(m, s);
+  }
+  const bool lo = lane < 16;
+  int s = 0;
+  uint32_t ph = 0;
+  for (long m = m0; m < M; m += stride) {
+    const int t = (int)(m % T);
+    float2 cs[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) cs[e] = tab[(long)t * half + (lane & 15) * E + e];
+    const float rl = lane < nh ? rstd_qk[m * nh + lane] : 0.f;
+    int none = 0;
+    if (!mbar_wait_bounded(&r.bars[s], ph, &none, err, SITE_QKNORM, timeout_ns)) {
+      armed[s] = -1;
+      ring_drain(r, armed, err, timeout_ns);
+      return;
+    }
+    const uint8_t* gs = r.slot(s) + lane * E * sizeof(A);
+    const uint8_t* zs = gs + nh * row;
+    A* grow = dqkv + m * (H + 2) * h + lane * E;
+    for (int j = 0; j < nh; ++j) {
+      float g[E], z[E];
+      load_vec_s<A, E>(gs + (size_t)j * row, g);
+      load_vec_s<A, E>(zs + (size_t)j * row, z);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot += g[e] * z[e];
+      const float mean = warp_sum(dot) / (float)h;
+      const float rr = j < 32 ? __shfl_sync(0xffffffffu, rl, j) : rstd_qk[m * nh + j];
+      float out[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float wv = g[e] - z[e] * mean;
+        const float pr = __shfl_xor_sync(0xffffffffu, wv, 16);
+        out[e] = rr * (lo ? (wv * cs[e].x + pr * cs[e].y) : (wv * cs[e].x - pr * cs[e].y));
+      }
+      store_vec<A, E>(grow + (size_t)j * h, out);
+    }
+    __syncwarp();
+    const long mn = m + kStages * stride;
+    if (mn < M) {
+      if (lane == 0) {
+        fence_proxy_async_shared();
+        fill(mn, s);
+      }
+    } else {
+      armed[s] = -1;
+    }
+    if (++s == kStages) { s = 0; ph ^= 1u; }
+  }
+}
+
 inline int row_blocks(long rows) { return (int)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock); }
+
+// Dynamic shared memory of a staged launch, or 0 when its slots do not fit.
+inline int staged_smem(long slot_bytes) {
+  const long bytes = slot_bytes * kStages * kStagedWarps;
+  return bytes <= 200 * 1024 ? (int)bytes : 0;
+}
+inline int staged_blocks(long M, int smem, int num_sms) {
+  const int per_sm = std::max(1, std::min(8, (int)((227L * 1024) / (smem + 1024))));
+  return (int)std::max<long>(1, std::min<long>((M + kStagedWarps - 1) / kStagedWarps,
+                                               (long)num_sms * per_sm));
+}
 
 }  // namespace
 
@@ -346,6 +493,25 @@ cudaError_t qknorm_rope_bwd(bool bf16, void* dqkv, const void* q, const void* k,
                             const float* rstd_qk, const float2* tab, int B, int T, int H, int h,
                             const Ctx& ctx) {
   const int M = B * T;
+  const int smem = staged_smem(2L * (H + 1) * h * (bf16 ? 2 : 4));
+  if (smem > 0) {
+    const int blocks = staged_blocks(M, smem, ctx.num_sms);
+    cudaError_t e = cudaSuccess;
+#define NC_QKBS(TA, EE)                                                                         \
+  e = cudaFuncSetAttribute(qknorm_rope_bwd_staged_kernel<TA, EE>,                            \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);               \
+  if (e != cudaSuccess) return e;                                                            \
+  qknorm_rope_bwd_staged_kernel<TA, EE><<<blocks, 32 * kStagedWarps, smem, ctx.stream>>>(    \
+      static_cast<TA*>(dqkv), static_cast<const TA*>(q), static_cast<const TA*>(k), rstd_qk,  \
+      tab, M, T, H, ctx.err, ctx.timeout_ns)
+    if (bf16) {
+      if (h == 128) { NC_QKBS(nc::bf16, 4); } else { NC_QKBS(nc::bf16, 2); }
+    } else {
+      if (h == 128) { NC_QKBS(float, 4); } else { NC_QKBS(float, 2); }
+    }
+#undef NC_QKBS
+    return launched(1);
+  }
   const int blocks = row_blocks(M);
 #define NC_QKB(TA, EE)                                                                      \
   qknorm_rope_bwd_kernel<TA, EE><<<blocks, 32 * kWarpsPerBlock, 0, ctx.stream>>>(          \

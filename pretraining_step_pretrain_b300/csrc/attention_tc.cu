@@ -16,12 +16,13 @@
 // columns in the backward passes (384 threads), four of 32 in the forward
 // (640 threads, four warps per scheduler).  Row reductions need no shuffles.
 // The probability-like operands (P in the forward, P^T and dS^T in the dK/dV
-// pass) go from registers to tensor memory as bf16 pairs and feed the next
-// MMA as its A operand; dS of the dQ pass goes to 128B-swizzled shared
-// memory.  A 64-wide [row][64 dims] swizzled tile is both a K-major operand
-// (rows = N) and an MN-major one (rows = K), so no operand is ever
-// transposed.  All mbarrier waits are bounded; on timeout the CTA records
-// DEV_TIMEOUT, stops, drains in-flight copies and MMAs, and frees TMEM.
+// pass, dS in the dQ pass) go from registers to tensor memory as bf16 pairs
+// and feed the next MMA as its A operand; the streamed Q, K, V, dO tiles stay
+// in 128B-swizzled shared memory as TMA delivers them.  A 64-wide [row][64
+// dims] swizzled tile is both a K-major operand (rows = N) and an MN-major one
+// (rows = K), so no operand is ever transposed.  All mbarrier waits are
+// bounded; on timeout the CTA records DEV_TIMEOUT, stops, drains in-flight
+// copies and MMAs, and frees TMEM.
 #include <algorithm>
 
 #include "nc_common.cuh"
@@ -43,20 +44,6 @@ constexpr int SITE_ATTN = 300;
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Store 64 bf16 values of one row into a [rows][64] 128B-swizzled atom.
-__device__ __forceinline__ void store_row_atom(uint8_t* atom, int row, const float* x) {
-  uint8_t* base = atom + row * 128;
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    uint4 q;
-    q.x = pack2(x[ch * 8 + 0], x[ch * 8 + 1]);
-    q.y = pack2(x[ch * 8 + 2], x[ch * 8 + 3]);
-    q.z = pack2(x[ch * 8 + 4], x[ch * 8 + 5]);
-    q.w = pack2(x[ch * 8 + 6], x[ch * 8 + 7]);
-    *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) = q;
-  }
 }
 
 // (x - d) * p on both halves of a packed fp32 pair: one instruction each for
@@ -452,9 +439,9 @@ constexpr int ATOM = 16384;                  // [128 rows][64] bf16
 constexpr int KVS = 2;                       // K/V ring stages (64 KB each)
 constexpr int K_OFF = 0;                     // KVS x 32 KB ([128 keys][128 dims] = 2 atoms)
 constexpr int V_OFF = K_OFF + KVS * 32768;   // KVS x 32 KB
-constexpr int DS_OFF = V_OFF + KVS * 32768;  // 2 x 32 KB ([128 rows][128 keys], by tile parity);
-                                             // first the staging of the Q and dO tiles
-constexpr int BAR_OFF = DS_OFF + 2 * 32768;
+constexpr int Q_OFF = V_OFF + KVS * 32768;   // 32 KB, the CTA's 128 rows
+constexpr int DO_OFF = Q_OFF + 32768;        // 32 KB
+constexpr int BAR_OFF = DO_OFF + 32768;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
 static_assert(SMEM <= 232448, "dQ pass shared memory exceeds 227 KB");
 }  // namespace bdq
@@ -471,13 +458,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* q_full = bars + 0;          // Q and dO in tensor memory (softmax warps)
-  uint64_t* kv_full = bars + 1;         // [KVS]
+  uint64_t* kv_full = bars + 1;         // [KVS] (bars + 0 is unused)
   uint64_t* kv_empty = bars + 1 + KVS;  // [KVS]
   uint64_t* s_full = bars + 1 + 2 * KVS;    // S and dP of the tile ready
   uint64_t* s_free = bars + 2 + 2 * KVS;    // copied out, one arrival per softmax warp
-  uint64_t* ds_full = bars + 3 + 2 * KVS;   // [2] by tile parity, one arrival per softmax warp
-  uint64_t* dq_done = bars + 5 + 2 * KVS;   // [2] by tile parity
+  uint64_t* ds_full = bars + 3 + 2 * KVS;   // [2] by dS buffer, one arrival per softmax warp
+  uint64_t* dq_done = bars + 5 + 2 * KVS;   // [2] by dS buffer: the dQ MMA that read it is done
   uint64_t* drain = bars + 7 + 2 * KVS;
   uint64_t* qd_full = bars + 8 + 2 * KVS;   // Q and dO tiles staged (TMA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9 + 2 * KVS);
@@ -492,7 +478,6 @@ __global__ void __launch_bounds__(NT, 1)
   const int nkv = t_last / BKV + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, NSW);
     for (int i = 0; i < KVS; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -517,15 +502,16 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const CtaSync sync{abort_flag, err, timeout_ns};
-  // TMEM columns: S at 0, dP at 128, dQ at 256, Q at 384, dO at 448 (bf16 pairs).
+  // TMEM columns: S at 0, dP at 128, dQ at 256, dS at 384 and 448 (bf16 pairs,
+  // by tile parity).
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer (Q, dO; K, V)
     mbar_arrive_expect_tx(qd_full, 4 * ATOM);
-    tma_load_3d(smem + DS_OFF, &tmQ, qd_full, 0, (int)r0, b);
-    tma_load_3d(smem + DS_OFF + ATOM, &tmQ, qd_full, 64, (int)r0, b);
-    tma_load_3d(smem + DS_OFF + 32768, &tmDO, qd_full, 0, (int)r0, b);
-    tma_load_3d(smem + DS_OFF + 32768 + ATOM, &tmDO, qd_full, 64, (int)r0, b);
+    tma_load_3d(smem + Q_OFF, &tmQ, qd_full, 0, (int)r0, b);
+    tma_load_3d(smem + Q_OFF + ATOM, &tmQ, qd_full, 64, (int)r0, b);
+    tma_load_3d(smem + DO_OFF, &tmDO, qd_full, 0, (int)r0, b);
+    tma_load_3d(smem + DO_OFF + ATOM, &tmDO, qd_full, 64, (int)r0, b);
     int armed[KVS];
     for (int i = 0; i < KVS; ++i) armed[i] = -1;
     for (int j = 0; j < nkv; ++j) {
@@ -557,10 +543,11 @@ __global__ void __launch_bounds__(NT, 1)
     const uint64_t dKk = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);    // K-major
     const uint64_t dKm = sdesc_sw128(smem_u32(smem + K_OFF), ATOM, 1024);  // MN-major
     const uint64_t dVk = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
-    const uint64_t dSk = sdesc_sw128(smem_u32(smem + DS_OFF), 16, 1024);
+    const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+    const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
     auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
     auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
-    bool ok = sync.wait(q_full, 0), issued = false;
+    bool ok = sync.wait(qd_full, 0), issued = false;
     // S(j) and dP(j) into their TMEM buffers once tile j - 1's copies are out.
     auto issue_s = [&](int j) -> bool {
       const int ks = j % KVS;
@@ -570,8 +557,8 @@ __global__ void __launch_bounds__(NT, 1)
       const uint64_t bk = dKk + ks * kStage, bv = dVk + ks * kStage;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
-        umma_bf16_tmem_a(tmem + 0, tmem + 384 + kk * 8, bk + koff(kk), idS, kk > 0 ? 1u : 0u);
-        umma_bf16_tmem_a(tmem + 128, tmem + 448 + kk * 8, bv + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_bf16(tmem + 0, dQk + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_bf16(tmem + 128, dOk + koff(kk), bv + koff(kk), idS, kk > 0 ? 1u : 0u);
       }
       umma_commit(s_full);
       issued = true;
@@ -582,10 +569,11 @@ __global__ void __launch_bounds__(NT, 1)
       const int ks = j % KVS, db = j & 1;
       if (!sync.wait(&ds_full[db], (j >> 1) & 1)) return false;
       tc_fence_after();
-      const uint64_t a = dSk + db * kStage, bk = dKm + ks * kStage;
+      const uint64_t bk = dKm + ks * kStage;
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, a + koff(kk), bk + moff(kk), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16_tmem_a(tmem + 256, tmem + 384 + db * 64 + kk * 8, bk + moff(kk), idQ,
+                         (j > 0 || kk > 0) ? 1u : 0u);
       umma_commit(&dq_done[db]);
       umma_commit(&kv_empty[ks]);
       return true;
@@ -613,31 +601,9 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
     const long grow = (long)b * TH + r;
-    // This thread's halves of the Q and dO rows, staged by TMA in swizzled
-    // [128 rows][64] atoms, into tensor memory (the A operands of every S and
-    // dP MMA); rows past the sequence were filled with zeros.
     const float dl = valid ? delta[grow] : 0.f;
     const float lse2 = valid ? lse[grow] * kLog2e : 0.f;
-    bool ok = sync.wait(qd_full, 0);
-    if (ok) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint8_t* src = smem + DS_OFF + m * 32768 + half * ATOM + row * 128;
-        float v[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
-          v[c * 4 + 0] = __uint_as_float(w.x);
-          v[c * 4 + 1] = __uint_as_float(w.y);
-          v[c * 4 + 2] = __uint_as_float(w.z);
-          v[c * 4 + 3] = __uint_as_float(w.w);
-        }
-        tmem_st_32cols(tmem + lane_off + 384 + m * 64 + half * 32, v);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
+    bool ok = true;
     // Rows of this CTA hold tokens t0 .. t_last; a key tile needs the mask
     // only where it reaches past t0 (or the tile has rows past the sequence).
     const int t0 = (int)(r0 / H);
@@ -667,11 +633,14 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int i = 0; i < 64; i += 2) sub_mul2(s[i], s[i + 1], dp[i], dp[i + 1], dl, dl, s[i], s[i + 1]);
       const int db = j & 1;
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack2(s[2 * i], s[2 * i + 1]);
       if (j > 1) {  // the dQ MMA of tile j - 2 has read this dS buffer
         if (!sync.wait(&dq_done[db], ((j >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
       }
-      store_row_atom(smem + DS_OFF + db * 32768 + half * ATOM, row, s);
-      fence_proxy_async_smem();
+      pairs_to_tmem(tmem + lane_off + 384 + db * 64 + half * 32, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[db]);

@@ -407,9 +407,10 @@ __global__ void __launch_bounds__(32 * kStagedWarps)
 inline int row_blocks(long rows) { return (int)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock); }
 
 // Dynamic shared memory of a staged launch, or 0 when its slots do not fit.
+constexpr int kStagedMaxSmem = 200 * 1024;
 inline int staged_smem(long slot_bytes) {
   const long bytes = slot_bytes * kStages * kStagedWarps;
-  return bytes <= 200 * 1024 ? (int)bytes : 0;
+  return bytes <= kStagedMaxSmem ? (int)bytes : 0;
 }
 inline int staged_blocks(long M, int smem, int num_sms) {
   const int per_sm = std::max(1, std::min(8, (int)((227L * 1024) / (smem + 1024))));
@@ -471,6 +472,24 @@ cudaError_t cast_f32_to_act(bool bf16, const float* x, void* y, long n, const Ct
   return launched(1);
 }
 
+template <typename A, int E>
+cudaError_t qknorm_bwd_staged(void* dqkv, const void* q, const void* k, const float* rstd_qk,
+                              const float2* tab, int M, int T, int H, int blocks, int smem,
+                              const Ctx& ctx) {
+  static bool attr = false;  // the opt-in shared-memory limit, set once per instantiation
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(qknorm_rope_bwd_staged_kernel<A, E>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStagedMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  qknorm_rope_bwd_staged_kernel<A, E><<<blocks, 32 * kStagedWarps, smem, ctx.stream>>>(
+      static_cast<A*>(dqkv), static_cast<const A*>(q), static_cast<const A*>(k), rstd_qk, tab, M,
+      T, H, ctx.err, ctx.timeout_ns);
+  return launched(1);
+}
+
 cudaError_t qknorm_rope_fwd(bool bf16, const void* qkv, const float2* tab, void* q, void* k,
                             void* v, float* rstd_qk, int B, int T, int H, int h, float eps,
                             const Ctx& ctx) {
@@ -496,21 +515,12 @@ cudaError_t qknorm_rope_bwd(bool bf16, void* dqkv, const void* q, const void* k,
   const int smem = staged_smem(2L * (H + 1) * h * (bf16 ? 2 : 4));
   if (smem > 0) {
     const int blocks = staged_blocks(M, smem, ctx.num_sms);
-    cudaError_t e = cudaSuccess;
-#define NC_QKBS(TA, EE)                                                                         \
-  e = cudaFuncSetAttribute(qknorm_rope_bwd_staged_kernel<TA, EE>,                            \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);               \
-  if (e != cudaSuccess) return e;                                                            \
-  qknorm_rope_bwd_staged_kernel<TA, EE><<<blocks, 32 * kStagedWarps, smem, ctx.stream>>>(    \
-      static_cast<TA*>(dqkv), static_cast<const TA*>(q), static_cast<const TA*>(k), rstd_qk,  \
-      tab, M, T, H, ctx.err, ctx.timeout_ns)
     if (bf16) {
-      if (h == 128) { NC_QKBS(nc::bf16, 4); } else { NC_QKBS(nc::bf16, 2); }
-    } else {
-      if (h == 128) { NC_QKBS(float, 4); } else { NC_QKBS(float, 2); }
+      if (h == 128) return qknorm_bwd_staged<nc::bf16, 4>(dqkv, q, k, rstd_qk, tab, M, T, H, blocks, smem, ctx);
+      return qknorm_bwd_staged<nc::bf16, 2>(dqkv, q, k, rstd_qk, tab, M, T, H, blocks, smem, ctx);
     }
-#undef NC_QKBS
-    return launched(1);
+    if (h == 128) return qknorm_bwd_staged<float, 4>(dqkv, q, k, rstd_qk, tab, M, T, H, blocks, smem, ctx);
+    return qknorm_bwd_staged<float, 2>(dqkv, q, k, rstd_qk, tab, M, T, H, blocks, smem, ctx);
   }
   const int blocks = row_blocks(M);
 #define NC_QKB(TA, EE)                                                                      \

@@ -21,6 +21,11 @@ def _built():
 
 
 RAGGED = nc_synth.ModelShape(depth=2, d_model=256, n_head=2, head_dim=128, d_mlp=512, vocab=4160)
+# Many heads: the QK-norm + RoPE backward's per-warp staging slots no longer
+# fit in shared memory (fp32 from 16 heads, bf16 from 33), so these take its
+# register path.
+WIDE_F32 = nc_synth.ModelShape(depth=1, d_model=128, n_head=20, head_dim=128, d_mlp=128, vocab=256)
+WIDE_BF16 = nc_synth.ModelShape(depth=1, d_model=128, n_head=36, head_dim=128, d_mlp=128, vocab=256)
 
 
 @pytest.mark.parametrize("case", [
@@ -32,6 +37,8 @@ RAGGED = nc_synth.ModelShape(depth=2, d_model=256, n_head=2, head_dim=128, d_mlp
     ("small_bf16", nc_synth.SMALL.shape, 8, 256, "bf16", "zipf", ()),
     ("ragged_bf16", RAGGED, 3, 100, "bf16", "zipf", ()),
     ("tiny_len1_bf16", RAGGED, 2, 1, "bf16", "zipf", ()),
+    ("wide_heads_f32", WIDE_F32, 2, 24, "f32", "uniform", ()),
+    ("wide_heads_bf16", WIDE_BF16, 2, 40, "bf16", "zipf", ()),
 ], ids=lambda c: c[0])
 def test_step_matches_oracle(case):
     name, shape, B, T, dtype, dist, zero = case

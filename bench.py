@@ -251,6 +251,32 @@ def config_dict(w, n):
             "l2": "no flush: working set far larger than L2"}
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+def rank_batch(w, rank):
+    """This rank's shard of the job: its own B x T token rows (seed = rank);
+    every rank holds the same weights."""
+    return nc_synth.make_tokens(w.shape.vocab, w.batch, w.seq, seed=rank, dist=w.ids)
+
+
+def max_over_ranks(x, world):
+    """The slowest rank's value, returned on every rank (x when world == 1).
+    The tensor lives where the process group's backend wants it: the GPU for
+    NCCL, the host for gloo."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(B, T, world, steps, seconds):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return B * T * world * steps / seconds
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -259,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
     w = nc_synth.WORKLOADS[args.workload]
     shape, B, T = w.shape, w.batch, w.seq
     weights = nc_synth.make_weights(shape, seed=1, bf16=(w.dtype == "bf16"))
-    ids, tg = nc_synth.make_tokens(shape.vocab, B, T, seed=rank, dist=w.ids)
+    ids, tg = rank_batch(w, rank)
     st = nc.Step(shape, w.dtype, B, T, weights, device=f"cuda:{local_rank}")
     ids_d = torch.from_numpy(ids).cuda()
     tg_d = torch.from_numpy(tg).cuda()
@@ -298,16 +324,11 @@ def run_ours(args, rank, world, local_rank):
     recs = nc.profile_stop()
     clk = clocks.stop()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
     if st.status() != 0:
         raise RuntimeError("device error during the timed steps")
     loss = float(st.loss.item())
-    tokens = B * T * world * args.steps
-    value = tokens / (ms / 1000.0)
+    value = job_tokens_per_s(B, T, world, args.steps, ms / 1000.0)
 
     # end to end through the public call with host buffers
     ids_h = torch.from_numpy(ids).pin_memory()
@@ -317,13 +338,9 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         st.run_host(ids_h, tg_h)
-    t_e2e = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e = {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
-           "d2h_bytes_per_step": 4}
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": job_tokens_per_s(B, T, world, args.steps, t_e2e), "unit": "tokens/s",
+           "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4}
 
     # per-launch-group attribution over the timed steps
     rows, prof_total = aggregate_profile(recs)

@@ -253,6 +253,24 @@ nc_status nc_gemm_batched(int dtype, int layout, int epilogue, int batch, int M,
                           long b_bstride, void* C, int ldc, long c_bstride, const void* aux,
                           float alpha, float beta, void* ws, size_t ws_bytes, void* stream);
 
+/* 8-bit floating-point contraction on the same tensor-core kernel (the FP8
+ * mixed-precision training of the latest version: nanochat hub page, core
+ * technical highlights.  The pages name no format; this is OCP FP8 E4M3 --
+ * 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * S.1111.111 is NaN, largest finite 448):
+ *   C(M,N) = scale * A(M,K) . B(N,K)^T
+ * A, B: E4M3 codes as raw bytes, row-major, both K-major (layout NT only),
+ * leading dimensions lda, ldb in elements (= bytes), multiples of 16;
+ * products are exact and accumulate in fp32; scale (finite) is applied to the
+ * fp32 sum, e.g. the product of the operands' per-tensor dequantisation
+ * scales.  out_dtype NC_BF16 or NC_F32 selects C's type; ldc in elements, a
+ * multiple of 8.  M, N, K >= 1, N % 32 == 0, K % 16 == 0 (M ragged).  No
+ * workspace beyond the error word (ws >= 256 B); pointers 16-byte aligned.
+ * The step itself stays bf16. */
+nc_status nc_gemm_fp8(int M, int N, int K, const void* A, int lda, const void* Bm, int ldb,
+                      int out_dtype, void* C, int ldc, float scale, void* ws, size_t ws_bytes,
+                      void* stream);
+
 /* Causal multi-query attention alone (architecture list: MQA; causal from the
  * next-token objective).  q (B, T, H, h), k and v (B, T, h), o (B, T, H, h),
  * act type; lse float32 (B, T, H): natural-log sum of exp of the scaled

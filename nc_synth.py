@@ -124,3 +124,15 @@ def make_weights(shape: ModelShape, seed: int = 1, bf16: bool = True,
             w[:] = 0.0
         out[name] = round_to_bf16(w) if bf16 else w
     return out
+
+
+def make_e4m3_codes(rows: int, cols: int, seed: int, exp_lo: int = 3, exp_hi: int = 10):
+    """Random 8-bit codes laid out as s.eeee.mmm (uint8, (rows, cols)): sign and
+    mantissa fields uniform, exponent field uniform in [exp_lo, exp_hi], so no
+    code is NaN and the magnitudes stay within a few powers of two of 1.  Bit
+    fields only -- the values the codes stand for are the oracle's business."""
+    rng = np.random.default_rng(seed)
+    s = rng.integers(0, 2, size=(rows, cols), dtype=np.uint8)
+    e = rng.integers(exp_lo, exp_hi + 1, size=(rows, cols), dtype=np.uint8)
+    m = rng.integers(0, 8, size=(rows, cols), dtype=np.uint8)
+    return (s << 7) | (e << 3) | m

@@ -53,6 +53,32 @@ struct EpiStore {
   __device__ __forceinline__ void row_end(int, int, float) const {}
 };
 
+// Scaled store: C = scale * acc (the dequantisation of a product of 8-bit
+// operands: scale = s_A s_B).
+template <typename TOut>
+struct EpiScaleStore {
+  static constexpr bool kRowReduce = false;
+  using Out = TOut;
+  TOut* c;
+  long ldc;
+  float scale;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  template <int W>
+  __device__ __forceinline__ float compute(int, int, float (&v)[W], int) const {
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] *= scale;
+    return 0.f;
+  }
+  template <int W>
+  __device__ __forceinline__ float apply(int row, int col, float (&v)[W], int) const {
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] *= scale;
+    store_row_chunk<TOut, W>(c + (long)row * ldc + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+};
+
 // Float32 store for weight gradients.  With split-K each split writes its own
 // slab (c + split * split_stride) and a reduction kernel sums the slabs in a
 // fixed order; with one split the epilogue writes (or accumulates into) C.

@@ -193,16 +193,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 // stride `ld` and matrix stride `bstride` elements (dims {inner, outer, nb});
 // 128-byte swizzle; out-of-range elements read as zero.
 bool make_tmap(CUtensorMap* m, const void* base, long inner, long outer, long ld, int box_inner,
-               int box_outer, long nb = 1, long bstride = 0) {
+               int box_outer, long nb = 1, long bstride = 0, bool bytes = false) {
   auto enc = tmap_encoder();
   if (!enc) return false;
   if (nb < 1) nb = 1;
   if (bstride <= 0) bstride = outer * ld;
+  const long es = bytes ? 1 : 2;  // 8-bit (E4M3 as raw bytes) or bf16 elements
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)nb};
-  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(bstride * es)};
   cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -266,6 +268,33 @@ cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* ou
   return launched(1);
 }
 
+// C(M,N) = scale * A(M,K) . B(N,K)^T with E4M3 operands (both K-major, as
+// raw bytes), fp32 accumulation, bf16 or fp32 output.
+template <class Epi>
+cudaError_t launch_tc_fp8(const GemmArgs& g, const Epi& epi, const Ctx& ctx) {
+  // A k-block is 128 bytes of a row (128 values); the planner counts k-blocks
+  // of 64 elements, so it gets K / 2 (K is a multiple of 16).
+  const Plan p = make_plan(GEMM_NT, EPI_STORE, g.M, g.N, g.K / 2, g.group_m);
+  CUtensorMap ta, tb, tcm;
+  bool ok = make_tmap(&ta, g.A, g.K, g.M, g.lda, 128, tc::HALF_ROWS, 1, 0, true) &&
+            make_tmap(&tb, g.B, g.K, g.N, g.ldb, 128, tc::HALF_ROWS, 1, 0, true) &&
+            make_tmap_out<typename Epi::Out>(&tcm, g.C, g.N, g.M, g.ldc, 1, 0);
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = tc::gemm_bf16_tc_kernel<false, false, Epi, true>;
+  constexpr int smem_bytes = tc::SmemPlan<false>::BYTES;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = 2 * std::max(1, std::min(p.sch.units, ctx.num_sms / 2));
+  kern<<<grid, tc::NUM_THREADS, smem_bytes, ctx.stream>>>(ta, tb, tcm, tcm, p.sch, g.M, g.N, epi,
+                                                          ctx.err, ctx.timeout_ns);
+  return launched(1);
+}
+
 template <class Epi>
 cudaError_t dispatch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* out, long ldo,
                         long zslabs, const Ctx& ctx) {
@@ -323,6 +352,12 @@ cudaError_t splitk_reduce(float* c, const float* slabs, int splits, long n, int 
 size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K) {
   Plan p = make_plan(layout, epi, M, N, K, 0);
   return p.sch.splits > 1 ? (size_t)p.sch.splits * M * N : 0;
+}
+
+cudaError_t gemm_fp8(const GemmArgs& g, bool out_f32, float scale, const Ctx& ctx) {
+  if (out_f32)
+    return launch_tc_fp8(g, EpiScaleStore<float>{static_cast<float*>(g.C), g.ldc, scale}, ctx);
+  return launch_tc_fp8(g, EpiScaleStore<bf16>{static_cast<bf16*>(g.C), g.ldc, scale}, ctx);
 }
 
 cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx) {

@@ -112,6 +112,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+// kind::f8f6f4 with both operands E4M3 (format code 0 in bits 7-9 and 10-12),
+// both K-major, fp32 accumulator (bits 4-5 = 1).
+__host__ __device__ constexpr uint32_t idesc_e4m3() {
+  return (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+// One k-block is 128 bytes of every operand row: 64 bf16 or 128 E4M3 values.
+template <bool kFp8>
+__host__ __device__ constexpr int kblock_elems() { return kFp8 ? 128 : BK; }
 
 // Epilogues that declare kAuxTma read a second operand with C's layout
 // (ReLU^2 backward: the saved activation; AXPBY: the addend); the kernel
@@ -175,13 +183,14 @@ __device__ __forceinline__ void unstage_row(const uint8_t* chunk, int r, float (
   }
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, bool kFp8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmAux, const Sched sch, const int M,
                         const int N, const Epi epi, int* err, const long long timeout_ns) {
+  static_assert(!kFp8 || (!A_MN && !B_MN), "8-bit operands are K-major");
   constexpr bool kAux = HasAuxTma<Epi>::value;
   using Plan = SmemPlan<kAux>;
   constexpr int STAGES = Plan::kStages;
@@ -263,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
         uint8_t* a = sA + stage * A_BYTES;
         uint8_t* b = sB + stage * B_BYTES;
-        const int k0 = kb * BK;
+        const int k0 = kb * kblock_elems<kFp8>();
         if (!A_MN) {
           tma_load_3d_pair(a, &tmA, bar, k0, row_a, batch);
         } else {
@@ -296,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (even CTA) ----------------
-    constexpr uint32_t idesc = idesc_bf16(A_MN, B_MN);
+    constexpr uint32_t idesc = kFp8 ? idesc_e4m3() : idesc_bf16(A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -325,7 +334,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int k = 0; k < BK / 16; ++k) {
           const uint64_t ad = A_MN ? desc_mnmajor(a_addr, k) : desc_kmajor(a_addr, k);
           const uint64_t bd = B_MN ? desc_mnmajor(b_addr, k) : desc_kmajor(b_addr, k);
-          umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          if constexpr (kFp8)  // K = 32 E4M3 values: the same 32 bytes per step
+            umma_f8_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          else
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
         }
         issued = true;
         umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs

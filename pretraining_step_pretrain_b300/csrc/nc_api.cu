@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <atomic>
 #include <string>
@@ -624,6 +625,30 @@ nc_status nc_gemm(int dtype, int layout, int epilogue, int M, int N, int K, cons
   const Ctx ctx = make_ctx(ws, stream);
   cudaError_t e = dtype == NC_BF16 ? gemm_bf16(g, ctx) : gemm_f32(g, ctx);
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  return NC_OK;
+}
+
+nc_status nc_gemm_fp8(int M, int N, int K, const void* A, int lda, const void* Bm, int ldb,
+                      int out_dtype, void* C, int ldc, float scale, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (out_dtype != NC_BF16 && out_dtype != NC_F32)
+    return fail(NC_ERR_INVALID_ARG, "bad output dtype %d", out_dtype);
+  if (M < 1 || N < 1 || K < 1 || N % 32 || K % 16)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE,
+                "M=%d N=%d K=%d: need >= 1, N %% 32 == 0 and K %% 16 == 0", M, N, K);
+  if (lda % 16 || ldb % 16 || ldc % 8)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE,
+                "lda, ldb must be multiples of 16 and ldc a multiple of 8");
+  if (lda < K || ldb < K || ldc < N)
+    return fail(NC_ERR_UNSUPPORTED_SHAPE, "leading dimension smaller than the row length");
+  if (!std::isfinite(scale)) return fail(NC_ERR_INVALID_ARG, "scale must be finite");
+  nc_status s = check_ptrs({A, Bm, C, ws});
+  if (s != NC_OK) return s;
+  if (ws_bytes < 256) return fail(NC_ERR_WORKSPACE, "gemm workspace too small");
+  GemmArgs g = gemm_args(NC_GEMM_NT, NC_EPI_STORE, M, N, K, A, lda, Bm, ldb, C, ldc);
+  const Ctx ctx = make_ctx(ws, stream);
+  cudaError_t e = gemm_fp8(g, out_dtype == NC_F32, scale, ctx);
+  if (e != cudaSuccess) return fail(NC_ERR_CUDA, "fp8 gemm launch: %s", cudaGetErrorString(e));
   return NC_OK;
 }
 

@@ -63,6 +63,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* 
 constexpr int kTileN = 256;            // n-tile width (per-row CE partials)
 size_t gemm_bf16_split_elems(int layout, int epi, int M, int N, int K);
 cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx);
+// E4M3 operands (layout NT, K-major raw bytes), C = scale * A B^T, bf16 or fp32 out.
+cudaError_t gemm_fp8(const GemmArgs& g, bool out_f32, float scale, const Ctx& ctx);
 // fp32 SIMT path (debug / parity mode).
 cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx);
 

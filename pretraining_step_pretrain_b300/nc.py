@@ -29,7 +29,7 @@ EXPORTS = ("nc_workspace_bytes", "nc_embed_norm", "nc_block_fwd", "nc_lmhead_sof
            "nc_attention_bwd_noalloc",
            "nc_launch_count", "nc_profile_start", "nc_profile_stop", "nc_profile_record",
            "nc_selftest_wait_timeout", "nc_gemm_batched", "nc_optimizer_workspace_bytes",
-           "nc_optimizer_step", "nc_eval")
+           "nc_optimizer_step", "nc_eval", "nc_gemm_fp8")
 
 
 class NcConfig(ctypes.Structure):
@@ -118,6 +118,7 @@ def lib() -> ctypes.CDLL:
                                     P, I, ctypes.c_long, P, ctypes.c_float, ctypes.c_float, P, S,
                                     P]),
             "nc_optimizer_workspace_bytes": (S, [C]),
+            "nc_gemm_fp8": (I, [I, I, I, P, I, P, I, I, P, I, ctypes.c_float, P, S, P]),
             "nc_eval": (I, [C, I, I, P, P, P, P, ctypes.POINTER(NcLayerW), P, P, P, S, P]),
             "nc_optimizer_step": (I, [C, ctypes.POINTER(NcOptConfig), I, ctypes.c_float, P, P,
                                       ctypes.POINTER(NcLayerF), P, P, ctypes.POINTER(NcLayerWC),
@@ -211,6 +212,19 @@ def step(cfg, B, T, ids, targets, wte, layers, w_lm, loss, dwte, grads, dw_lm, a
 def get_device_status(ws) -> int:
     p, _ = _ws(ws)
     return lib().nc_get_device_status(p, _stream())
+
+
+def gemm_fp8(M, N, K, A, lda, B, ldb, C, ldc, scale=1.0, ws=None):
+    """C = scale * A B^T on E4M3 operands given as uint8 tensors of codes (see
+    nc_gemm_fp8); C's dtype (bfloat16 or float32) selects the output type."""
+    import torch
+    out = NC_F32 if C.dtype == torch.float32 else NC_BF16
+    if ws is None:
+        ws = alloc_workspace(256, A.device)
+    p, n = _ws(ws)
+    _check(lib().nc_gemm_fp8(M, N, K, _ptr(A), lda, _ptr(B), ldb, out, _ptr(C), ldc,
+                             float(scale), p, n, _stream()))
+    return ws
 
 
 def gemm(dtype, layout, epilogue, M, N, K, A, lda, B, ldb, C, ldc, aux=None, accumulate=0,

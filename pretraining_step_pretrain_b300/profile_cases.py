@@ -5,6 +5,10 @@
         --M 16384 --N 5120 --K 1280 --iters 3
     python -m pretraining_step_pretrain_b300.profile_cases attn --B 4 --T 2048 --H 10 --bwd
     python -m pretraining_step_pretrain_b300.profile_cases step --workload small_bf16
+    python -m pretraining_step_pretrain_b300.profile_cases gemm_fp8 --M 65536 --N 5120 --K 1280
+
+The gemm and gemm_fp8 cases also print the mean time and FLOP rate of their
+launches after the first (CUDA events on the launching stream).
 """
 from __future__ import annotations
 
@@ -38,11 +42,41 @@ def gemm(a):
     f32_out = E in (nc.EPI_STORE_F32, nc.EPI_ADD_F32)
     C = torch.zeros(M, N, device="cuda", dtype=torch.float32 if f32_out else bf)
     aux = torch.rand(M, N, generator=g, device="cuda").to(bf) if E == nc.EPI_RELU2_BWD else None
-    ws = None
-    for _ in range(a.iters):
-        ws = nc.gemm(nc.NC_BF16, L, E, M, N, K, A, lda, B, ldb, C, N, aux=aux, ws=ws)
+    ws = nc.gemm(nc.NC_BF16, L, E, M, N, K, A, lda, B, ldb, C, N, aux=aux)
+    ms = _timed(lambda: nc.gemm(nc.NC_BF16, L, E, M, N, K, A, lda, B, ldb, C, N, aux=aux, ws=ws),
+                a.iters - 1)
+    print(f"gemm {a.layout} {a.epi} M={M} N={N} K={K}: ok" + _rate(ms, 2.0 * M * N * K))
+
+
+def _timed(fn, n):
+    """Mean ms of n calls of fn, CUDA events on the current stream (None if n < 1)."""
+    if n < 1:
+        torch.cuda.synchronize()
+        return None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    print(f"gemm {a.layout} {a.epi} M={M} N={N} K={K}: ok")
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def _rate(ms, flop):
+    return "" if ms is None else f", {ms:.3f} ms per launch, {flop / ms * 1e-9:.0f} TFLOP/s"
+
+
+def gemm_fp8(a):
+    """C (bf16) = A . B^T with E4M3 operands (random codes, exponents 3..10)."""
+    import nc_synth
+    M, N, K = a.M, a.N, a.K
+    A = torch.from_numpy(nc_synth.make_e4m3_codes(M, K, seed=1)).cuda()
+    B = torch.from_numpy(nc_synth.make_e4m3_codes(N, K, seed=2)).cuda()
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = nc.gemm_fp8(M, N, K, A, K, B, K, C, N, 1.0 / 64)
+    ms = _timed(lambda: nc.gemm_fp8(M, N, K, A, K, B, K, C, N, 1.0 / 64, ws=ws), a.iters - 1)
+    print(f"gemm_fp8 NT M={M} N={N} K={K}: ok" + _rate(ms, 2.0 * M * N * K))
 
 
 def attn(a):
@@ -93,6 +127,11 @@ def main():
     p.add_argument("--N", type=int, default=5120)
     p.add_argument("--K", type=int, default=1280)
     p.add_argument("--iters", type=int, default=3)
+    p = sub.add_parser("gemm_fp8")
+    p.add_argument("--M", type=int, default=16384)
+    p.add_argument("--N", type=int, default=5120)
+    p.add_argument("--K", type=int, default=1280)
+    p.add_argument("--iters", type=int, default=3)
     p = sub.add_parser("attn")
     p.add_argument("--B", type=int, default=4)
     p.add_argument("--T", type=int, default=2048)
@@ -103,7 +142,7 @@ def main():
     p.add_argument("--workload", default="small_bf16")
     p.add_argument("--iters", type=int, default=2)
     a = ap.parse_args()
-    {"gemm": gemm, "attn": attn, "step": step}[a.case](a)
+    {"gemm": gemm, "gemm_fp8": gemm_fp8, "attn": attn, "step": step}[a.case](a)
 
 
 if __name__ == "__main__":

@@ -109,6 +109,20 @@ def test_gemm_argument_checks(lib):
     assert f(0, 0, 4, 128, 128, 64, 4096, 64, 4096, 64, 4096, 128, None, 0, 4096, 1 << 20, None) == 1
 
 
+def test_fp8_gemm_argument_checks(lib):
+    f = lib.nc_gemm_fp8
+    # M N K A lda B ldb out C ldc scale ws ws_bytes stream
+    assert f(128, 128, 24, 4096, 32, 4096, 32, 0, 4096, 128, 1.0, 4096, 1 << 20, None) == 2  # K % 16
+    assert f(128, 100, 64, 4096, 64, 4096, 64, 0, 4096, 128, 1.0, 4096, 1 << 20, None) == 2  # N % 32
+    assert f(128, 128, 64, 4096, 72, 4096, 64, 0, 4096, 128, 1.0, 4096, 1 << 20, None) == 2  # lda % 16
+    assert f(128, 128, 64, 4096, 48, 4096, 64, 0, 4096, 128, 1.0, 4096, 1 << 20, None) == 2  # lda < K
+    assert f(128, 128, 64, 4096, 64, 4096, 64, 5, 4096, 128, 1.0, 4096, 1 << 20, None) == 1  # out dtype
+    assert f(128, 128, 64, 4096, 64, 4096, 64, 0, 4096, 128, float("inf"), 4096, 1 << 20,
+             None) == 1                                                                       # scale
+    assert f(128, 128, 64, 4104, 64, 4096, 64, 0, 4096, 128, 1.0, 4096, 1 << 20, None) == 1  # misaligned
+    assert f(128, 128, 64, 4096, 64, 4096, 64, 0, 4096, 128, 1.0, 4096, 16, None) == 3       # tiny ws
+
+
 def test_attention_argument_checks(lib):
     f = lib.nc_attention_fwd
     assert f(0, 1, 64, 2, 64, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 2  # bf16 h=64

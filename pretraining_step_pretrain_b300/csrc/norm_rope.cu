@@ -310,8 +310,9 @@ struct WarpRing {
   __device__ uint8_t* slot(int s) const { return base + (size_t)s * slot_bytes; }
 };
 
-// On a timed-out wait: wait (bounded) for this warp's other copies in flight,
-// then the caller returns.
+// On a timed-out wait: wait (bounded) for this warp's other copies in flight
+// (armed[s]: the parity slot s's pending fill completes with, or -1), then the
+// caller returns.
 __device__ __forceinline__ void ring_drain(const WarpRing& r, const int (&armed)[kStages],
                                            int* err, long long timeout_ns) {
   int none = 0;
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(32 * kStagedWarps)
         fence_proxy_async_shared();
         fill(mn, s);
       }
+      armed[s] = (int)(ph ^ 1u);  // the parity this refill completes with
     } else {
       armed[s] = -1;
     }

@@ -29,6 +29,9 @@
  *  - M = B*T tokens; ids/targets are int32 (B, T).  targets < 0 are ignored.
  *  - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous and
  *    stream-ordered; they return after enqueueing work.
+ *  - One GPU per process: the library opts its kernels into large shared
+ *    memory once, on the device current at the first call (data-parallel
+ *    use runs one process per GPU).
  *  - Workspace: `ws` of at least nc_workspace_bytes(cfg, B, T) bytes, 256-byte
  *    aligned.  It carries state between the calls of one step: nc_embed_norm
  *    writes the RoPE table and embedding statistics, nc_block_fwd(l) saves

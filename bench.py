@@ -193,6 +193,21 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def host_cpu():
+    """The host the oracle ran on: CPU model name (from /proc/cpuinfo) and the
+    number of logical cores."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"model": model, "nproc": os.cpu_count() or 1}
+
+
 def oracle_tokens_per_s(shape, T, min_seconds, max_steps, weights=None):
     """Time the fp64 oracle on one row of T tokens at `shape` (host cores)."""
     import oracle
@@ -236,6 +251,7 @@ def run_reference(args, rank, world):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": config_dict(w, args.gpus),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                            "host": host_cpu(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
@@ -411,7 +427,8 @@ def run_ours(args, rank, world, local_rank):
         del st
         torch.cuda.empty_cache()
         v, threads, n = oracle_tokens_per_s(shape, args.cpu_tokens, 10.0, 3, weights)
-        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "host": host_cpu(),
+               "kind": "oracle",
                "sample": f"{w.name} widths, 1 row x {args.cpu_tokens} tokens, {n} timed "
                          f"oracle step(s) after one untimed"}
 

@@ -71,3 +71,8 @@ def test_config_block_names_the_workload():
     c = bench.config_dict(D20, 4)
     assert c["workload"] == "d20_bf16" and c["global_batch"] == 128 and c["seq_len"] == 2048
     assert c["n_kv_head"] == 1 and "no collective" in c["parallelism"]
+
+
+def test_host_cpu_names_model_and_cores():
+    h = bench.host_cpu()
+    assert h["nproc"] >= 1 and isinstance(h["model"], str) and h["model"]

@@ -87,7 +87,7 @@ def rope_bwd(dy: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
 def _causal_scores(q: np.ndarray, k: np.ndarray) -> np.ndarray:
     h = q.shape[-1]
     T = q.shape[1]
-    s = np.einsum("bthd,bjd->bhtj", q, k) / np.sqrt(h)
+    s = np.einsum("bthd,bjd->bhtj", q, k, optimize=True) / np.sqrt(h)
     future = np.triu(np.ones((T, T), dtype=bool), k=1)      # j > i
     return np.where(future[None, None], -np.inf, s)
 
@@ -100,18 +100,18 @@ def _softmax(s: np.ndarray) -> np.ndarray:
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     p = _softmax(_causal_scores(q, k))                      # (B, H, T, T)
-    return np.einsum("bhtj,bjd->bthd", p, v)
+    return np.einsum("bhtj,bjd->bthd", p, v, optimize=True)
 
 
 def attention_bwd(do: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray):
     """Gradients (dq, dk, dv); dk and dv sum over all query heads (MQA)."""
     h = q.shape[-1]
     p = _softmax(_causal_scores(q, k))
-    dv = np.einsum("bhtj,bthd->bjd", p, do)
-    dp = np.einsum("bthd,bjd->bhtj", do, v)
+    dv = np.einsum("bhtj,bthd->bjd", p, do, optimize=True)
+    dp = np.einsum("bthd,bjd->bhtj", do, v, optimize=True)
     ds = p * (dp - np.sum(dp * p, axis=-1, keepdims=True))
-    dq = np.einsum("bhtj,bjd->bthd", ds, k) / np.sqrt(h)
-    dk = np.einsum("bhtj,bthd->bjd", ds, q) / np.sqrt(h)
+    dq = np.einsum("bhtj,bjd->bthd", ds, k, optimize=True) / np.sqrt(h)
+    dk = np.einsum("bhtj,bthd->bjd", ds, q, optimize=True) / np.sqrt(h)
     return dq, dk, dv
 
 

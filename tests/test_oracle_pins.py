@@ -5,6 +5,7 @@ log_softmax), brute force on tiny inputs, and central differences.
 Each test names the part of the method it pins; a plausible mistake (dropped
 term, wrong sign or index, transposed operand) in that part fails it.
 """
+import dataclasses
 import json
 import math
 import os
@@ -251,6 +252,75 @@ def test_zero_output_projections_reduce_to_softmax_regression():
     for l in range(shape.depth):
         assert np.all(g[f"w_qkv.{l}"] == 0.0) and np.all(g[f"w_fc.{l}"] == 0.0)
         assert np.abs(g[f"w_o.{l}"]).max() > 1e-6 and np.abs(g[f"w_proj.{l}"]).max() > 1e-6
+
+
+# ------------------------------------------------------------------ where RoPE acts in forward()
+def _one_layer_cache(ids):
+    shape = dataclasses.replace(nc_synth.GRADCHECK, depth=1)
+    return shape, oracle.forward(shape, _tiny_params(shape, seed=21), ids)
+
+
+def _rotate_closed_form(x, h, base):
+    """Rotate x (B, T, [heads,] h) by position t = 0..T-1 of its own row, written
+    out from the rotary definition (pairs (i, i + h/2), angle t base^(-2i/h)),
+    without the oracle's tables."""
+    T = x.shape[1]
+    ang = np.array([[t * base ** (-2.0 * i / h) for i in range(h // 2)] for t in range(T)])
+    c, s = np.cos(ang), np.sin(ang)
+    if x.ndim == 4:
+        c, s = c[:, None, :], s[:, None, :]
+    x1, x2 = x[..., : h // 2], x[..., h // 2:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+def test_forward_rotates_queries_and_keys_at_each_rows_own_positions():
+    """Architecture list: rotary embeddings act on the (QK-normed) queries and
+    key at each token's position within its row, and nothing else is rotated.
+    Fails if q or k is left unrotated, v is rotated, or positions run on
+    across rows instead of restarting at 0."""
+    ids, _ = nc_synth.make_tokens(32, 3, 9, seed=31, dist="uniform")
+    shape, cache = _one_layer_cache(ids)
+    lc = cache["layers"][0]
+    H, h = shape.n_head, shape.head_dim
+    np.testing.assert_allclose(lc["qr"], _rotate_closed_form(lc["qn"], h, shape.rope_base),
+                               rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lc["kr"], _rotate_closed_form(lc["kn"], h, shape.rope_base),
+                               rtol=1e-12, atol=1e-14)
+    assert np.abs(lc["qr"][:, 1:] - lc["qn"][:, 1:]).max() > 1e-3   # really rotated
+    assert np.abs(lc["kr"][:, 1:] - lc["kn"][:, 1:]).max() > 1e-3
+    # v: the raw value rows of the projection, neither normed nor rotated
+    w = _tiny_params(shape, seed=21)["w_qkv.0"]
+    np.testing.assert_array_equal(lc["v"], lc["xn"] @ w[(H + 1) * h:].T)
+    o = oracle.attention(lc["qr"], lc["kr"], lc["v"]).reshape(lc["o"].shape)
+    np.testing.assert_array_equal(lc["o"], o)
+
+
+def test_forward_positions_restart_in_every_row():
+    """Two rows holding the same tokens give the same outputs: a position
+    counted across the batch (row b starting at b T) would rotate row 1
+    differently from row 0."""
+    ids, _ = nc_synth.make_tokens(32, 1, 11, seed=32, dist="uniform")
+    ids2 = np.concatenate([ids, ids], axis=0)
+    _, cache = _one_layer_cache(ids2)
+    np.testing.assert_array_equal(cache["layers"][0]["qr"][0], cache["layers"][0]["qr"][1])
+    np.testing.assert_array_equal(cache["s"][0], cache["s"][1])
+
+
+def test_forward_scores_of_a_constant_row_depend_on_relative_position_only():
+    """With one token repeated along a row, every position has the same normed
+    q and k, so after rotation the score q_i . k_j is a function of i - j
+    alone -- and not a constant, which it would be without rotation."""
+    ids = np.full((1, 12), 7, dtype=np.int32)
+    shape, cache = _one_layer_cache(ids)
+    lc = cache["layers"][0]
+    T = ids.shape[1]
+    for hd in range(shape.n_head):
+        s = lc["qr"][0, :, hd] @ lc["kr"][0].T                    # (T, T): query i, key j
+        for delta in range(T):
+            diag = np.array([s[i, i - delta] for i in range(delta, T)])
+            np.testing.assert_allclose(diag, diag[0], rtol=1e-12, atol=1e-13)
+        lagged = np.array([s[T - 1, T - 1 - delta] for delta in range(T)])
+        assert np.ptp(lagged) > 1e-3
 
 
 # ------------------------------------------------------------------ structure

@@ -11,10 +11,17 @@ embedding backward -- all weight gradients produced.  Inputs are synthetic
 the timed region starts.  The working set (~40 GB at d20) is far larger than
 the 126 MB L2, so no flush is needed between steps.
 
-For N > 1 (torchrun, one rank per GPU) every rank runs its own batch of the
-same shape: the step shards by batch rows with no data-path collective, so
+For N > 1 (one rank per GPU) every rank runs its own batch of the same
+shape: the step shards by batch rows with no data-path collective, so
 scaling is weak; the only collectives are the timing barrier and the max
-over ranks.  Rank 0 prints one JSON line.
+over ranks.  `--gpus N` without a launcher starts the N ranks itself
+(torch.distributed.run on 127.0.0.1); under a launcher WORLD_SIZE must equal
+N.  Rank 0 prints one JSON line.
+
+The headline is timed with nothing but the step on the stream.  A second,
+separate pass of the same number of steps records CUDA events around every
+named launch group; it gives the per-kernel attribution and the roofline of
+the dominant kernel.
 """
 from __future__ import annotations
 
@@ -208,21 +215,56 @@ def host_cpu():
     return {"model": model, "nproc": os.cpu_count() or 1}
 
 
-def oracle_tokens_per_s(shape, T, min_seconds, max_steps, weights=None):
-    """Time the fp64 oracle on one row of T tokens at `shape` (host cores)."""
+def oracle_tokens_per_s(shape, B, T, min_seconds, max_steps, weights=None, threads=None):
+    """Time the fp64 oracle's full step on B rows of T tokens at `shape` (host
+    cores; `threads` caps the BLAS threads, None leaves them all)."""
+    import contextlib
+
     import oracle
     if weights is None:
         weights = nc_synth.make_weights(shape, seed=1, bf16=True)
     P = {k: v.astype(np.float64) for k, v in weights.items()}
-    ids, tg = nc_synth.make_tokens(shape.vocab, 1, T, seed=0)
-    oracle.step(shape, P, ids, tg)                       # first touch of every buffer
-    times = []
-    t_all = time.perf_counter()
-    while len(times) < max_steps and (time.perf_counter() - t_all < min_seconds or not times):
-        t0 = time.perf_counter()
-        oracle.step(shape, P, ids, tg)
-        times.append(time.perf_counter() - t0)
-    return T * len(times) / sum(times), blas_threads(), len(times)
+    ids, tg = nc_synth.make_tokens(shape.vocab, B, T, seed=0)
+    limit = contextlib.nullcontext()
+    if threads is not None:
+        from threadpoolctl import threadpool_limits
+        limit = threadpool_limits(threads)
+    with limit:
+        used = blas_threads()
+        oracle.step(shape, P, ids, tg)                   # first touch of every buffer
+        times = []
+        t_all = time.perf_counter()
+        while len(times) < max_steps and (time.perf_counter() - t_all < min_seconds or not times):
+            t0 = time.perf_counter()
+            oracle.step(shape, P, ids, tg)
+            times.append(time.perf_counter() - t0)
+    return B * T * len(times) / sum(times), used, len(times)
+
+
+def cpu_baseline(w, weights, tokens, full_d20=False):
+    """The fp64 oracle on the host cores: the bench workload's widths on one
+    row of `tokens` tokens (all BLAS threads, then one thread), the tiny and
+    small configurations' full steps, and optionally one whole 2048-token row
+    at the depth-20 widths."""
+    v, threads, n = oracle_tokens_per_s(w.shape, 1, tokens, 5.0, 2, weights)
+    v1, _, n1 = oracle_tokens_per_s(w.shape, 1, tokens, 0.0, 1, weights, threads=1)
+    out = {"value": v, "unit": "tokens/s", "cores": threads, "host": host_cpu(),
+           "kind": "oracle",
+           "sample": f"{w.name} widths, 1 row x {tokens} tokens, {n} timed full oracle "
+                     f"step(s) (forward + backward, fp64) after one untimed",
+           "one_thread": {"value": v1, "unit": "tokens/s", "steps": n1},
+           "full_steps": {}}
+    for name in ("tiny_f32", "small_bf16"):
+        o = nc_synth.WORKLOADS[name]
+        tv, tt, tn = oracle_tokens_per_s(o.shape, o.batch, o.seq, 1.0, 5)
+        out["full_steps"][name] = {"value": tv, "unit": "tokens/s", "cores": tt, "steps": tn,
+                                   "batch": o.batch, "seq": o.seq}
+    if full_d20:
+        d20 = nc_synth.D20
+        tv, tt, tn = oracle_tokens_per_s(d20.shape, 1, d20.seq, 0.0, 1)
+        out["full_steps"]["d20_bf16_1x2048"] = {"value": tv, "unit": "tokens/s", "cores": tt,
+                                                "steps": tn, "batch": 1, "seq": d20.seq}
+    return out
 
 
 # ---------------------------------------------------------------- arms
@@ -319,32 +361,43 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     visible = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v]
     gpu_idx = local_rank
     if local_rank < len(visible) and visible[local_rank].isdigit():
         gpu_idx = int(visible[local_rank])
     clocks = ClockSampler(gpu_idx)
-    # Per-launch-group CUDA events (recorded by the library on the launching
-    # stream, events created beforehand) over the timed steps themselves.
-    nc.profile_start(60 * (shape.depth + 2) * args.steps)
+    # Headline: K steps with nothing else on the stream; one event after each
+    # step (for the median), none inside it.
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     clocks.start()
     n0 = nc.launch_count()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        st.run()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    launches = nc.launch_count() - n0
+    clk = clocks.stop()
+    barrier()
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world)
+    if st.status() != 0:
+        raise RuntimeError("device error during the timed steps")
+    loss = float(st.loss.item())
+    value = job_tokens_per_s(B, T, world, args.steps, ms / 1000.0)
+
+    # Attribution: a separate pass of K steps with CUDA events recorded by the
+    # library around every named launch group on the launching stream.
+    nc.profile_start(60 * (shape.depth + 2) * args.steps)
+    e0, e1 = ev[0], ev[-1]
     e0.record(stream)
     for _ in range(args.steps):
         st.run()
     e1.record(stream)
     torch.cuda.synchronize()
-    launches = nc.launch_count() - n0
     recs = nc.profile_stop()
-    clk = clocks.stop()
-    barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1), world)
-    if st.status() != 0:
-        raise RuntimeError("device error during the timed steps")
-    loss = float(st.loss.item())
-    value = job_tokens_per_s(B, T, world, args.steps, ms / 1000.0)
+    prof_ms = e0.elapsed_time(e1)
 
     # end to end through the public call with host buffers
     ids_h = torch.from_numpy(ids).pin_memory()
@@ -358,7 +411,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": job_tokens_per_s(B, T, world, args.steps, t_e2e), "unit": "tokens/s",
            "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4}
 
-    # per-launch-group attribution over the timed steps
+    # per-launch-group attribution over the profiled steps
     rows, prof_total = aggregate_profile(recs)
     peaks, peak_src = load_peaks()
     top = None
@@ -368,6 +421,8 @@ def run_ours(args, rank, world, local_rank):
             top = (name, tot, cnt, kind, amount)
             break
     roofline = None
+    where = (f"CUDA events around each launch of the group on its stream, over {args.steps} "
+             f"profiled steps run right after the headline steps")
     if top:
         name, tot, cnt, kind, amount = top
         per_launch_s = tot / cnt / 1000.0
@@ -378,7 +433,7 @@ def run_ours(args, rank, world, local_rank):
                         "unit": "TFLOP/s", "frac": achieved / peak,
                         "traffic": measured_traffic(name),
                         "peak_source": f"{peak_src} bf16 sustained", "share": tot / prof_total,
-                        "algorithmic_per_launch": amount}
+                        "algorithmic_per_launch": amount, "timing": where}
         else:
             achieved = amount / per_launch_s / 1e9
             peak = peaks["hbm_gbs"]
@@ -386,9 +441,9 @@ def run_ours(args, rank, world, local_rank):
                         "unit": "GB/s", "frac": achieved / peak,
                         "traffic": measured_traffic(name),
                         "peak_source": f"{peak_src} copy bandwidth", "share": tot / prof_total,
-                        "algorithmic_per_launch": amount}
+                        "algorithmic_per_launch": amount, "timing": where}
     kernels = []
-    for name, (tot, cnt) in rows[:12]:
+    for name, (tot, cnt) in rows[:16]:
         kind, amount = algorithmic_cost(name, shape, B, T)
         entry = {"name": name, "ms_per_step": tot / args.steps,
                  "share": tot / prof_total}
@@ -426,17 +481,14 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del st
         torch.cuda.empty_cache()
-        v, threads, n = oracle_tokens_per_s(shape, args.cpu_tokens, 10.0, 3, weights)
-        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "host": host_cpu(),
-               "kind": "oracle",
-               "sample": f"{w.name} widths, 1 row x {args.cpu_tokens} tokens, {n} timed "
-                         f"oracle step(s) after one untimed"}
+        cpu = cpu_baseline(w, weights, args.cpu_tokens, full_d20=args.cpu_full_d20)
 
     f_tok = flops.flops_per_token(shape, T)
     f_tok_causal = flops.flops_per_token(shape, T, causal_actual=True)
     per_gpu = value / world
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+           "ms_per_step_median": statistics.median(step_ms),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": w.dtype, "data": "synthetic: Zipf(1.1) token ids, N(0,1/fan_in) weights",
            "config": config_dict(w, world),
@@ -449,27 +501,76 @@ def run_ours(args, rank, world, local_rank):
                           "causal_actual_vs_measured_burst":
                               per_gpu * f_tok_causal / (peaks["bf16_tflops"] * 1e12),
                           "peak_source": peak_src},
-           "loss": loss, "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
+           "loss": loss, "roofline": roofline, "kernels": kernels,
+           "profiled_ms_per_step": prof_ms / args.steps, "cpu_baseline": cpu,
            "e2e": e2e, "gpu_launches": launches, "clocks": clk, "optimizer": optim}
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
-def main():
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n, argv):
+    """Run this script as n ranks on this node (torch.distributed.run,
+    rendezvous on 127.0.0.1); returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def launcher_check(rank, world):
+    """Host-only check of the rank layout (no GPU work, no timing): every rank
+    joins a gloo group and rank 0 prints the ranks it sees."""
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    got = [None] * world
+    dist.all_gather_object(got, {"rank": rank, "world": world,
+                                 "local_rank": int(os.environ.get("LOCAL_RANK", 0))})
+    if rank == 0:
+        print(json.dumps({"launcher_check": True, "n_gpus": world, "ranks": got}), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+    del torch
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="d20_bf16", choices=sorted(nc_synth.WORKLOADS))
-    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--cpu-full-d20", action="store_true",
+                    help="also time one whole 2048-token row of the oracle at the depth-20 widths")
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-optimizer", action="store_true")
-    args = ap.parse_args()
+    ap.add_argument("--launcher-check", action="store_true",
+                    help="start the ranks, report the rank layout, run nothing on a GPU")
+    args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(launch_ranks(args.gpus, argv))
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but the launcher started {world} rank(s)",
+              file=sys.stderr)
+        sys.exit(2)
+    if args.launcher_check:
+        launcher_check(rank, world)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

@@ -155,8 +155,6 @@ nc_status nc_step(const nc_config* cfg, int B, int T, const int32_t* ids,
                   const void* w_lm, float* loss, float* dwte, const nc_layer_g* grads,
                   float* dw_lm, int accumulate, void* ws, size_t ws_bytes, void* stream);
 
-/* Synchronises `stream`, reads the device error word of `ws`, clears it and
- * returns NC_OK, NC_ERR_TIMEOUT or NC_ERR_TOKEN_RANGE (or NC_ERR_CUDA). */
 /* Forward-only evaluation (walkthrough, pretraining section: the run
  * reports validation bits per byte -- the next-token loss normalised by the
  * bytes per token, comparable across tokenizers).  Runs the forward pass and
@@ -170,6 +168,8 @@ nc_status nc_eval(const nc_config* cfg, int B, int T, const int32_t* ids, const 
                   const int32_t* token_bytes, const void* wte, const nc_layer_w* layers,
                   const void* w_lm, float* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Synchronises `stream`, reads the device error word of `ws`, clears it and
+ * returns NC_OK, NC_ERR_TIMEOUT or NC_ERR_TOKEN_RANGE (or NC_ERR_CUDA). */
 nc_status nc_get_device_status(void* ws, void* stream);
 
 const char* nc_status_string(nc_status s);
@@ -307,11 +307,23 @@ nc_status nc_attention_bwd(int dtype, int B, int T, int H, int h, const void* q,
  * device current) and caches it; make that first call before any stream
  * capture.  Every call shares the array: calls that overlap on the GPU race,
  * so order them (one stream, or events).  Each call rewrites every scratch
- * entry it reads, so no clearing is needed between calls. */
+ * entry it reads, so no clearing is needed between calls.  Like the rest of
+ * the library it assumes one GPU per process (the kernels' shared-memory
+ * opt-in is made once, on the first device used).
+ * Device-side conditions: the kernels bound every wait; a wait that runs out
+ * makes its CTA stop early, so dq/dk/dv of that call are incomplete, and
+ * records NC_ERR_TIMEOUT in a second fixed device word of the library (there
+ * is no workspace to hold it).  nc_attention_bwd_noalloc_status() reads it. */
 nc_status nc_attention_bwd_noalloc(int dtype, int B, int T, int H, int h, const void* q,
                                    const void* k, const void* v, const void* o,
                                    const float* lse, const void* dout, void* dq, int ldq,
                                    void* dk, int ldk, void* dv, int ldv, void* stream);
+
+/* Status of the allocation-free calls on the current device: synchronises
+ * `stream`, reads the device error word they share, clears it and returns
+ * NC_OK, NC_ERR_TIMEOUT (some call since the last read stopped early and left
+ * its gradients incomplete) or NC_ERR_CUDA.  Allocates nothing. */
+nc_status nc_attention_bwd_noalloc_status(void* stream);
 
 /* ---- measurement ----------------------------------------------------------
  * Support for the throughput and roofline measurements of the step (the
@@ -332,7 +344,9 @@ nc_status nc_profile_record(int i, const char** name, float* ms);
 
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier nothing will complete, for at most `timeout_us` microseconds, then
- * records NC_ERR_TIMEOUT in ws's error word and returns.  Never hangs. */
+ * records NC_ERR_TIMEOUT in ws's error word and returns.  Never hangs.  With
+ * ws == NULL it records into the allocation-free calls' error word instead
+ * (read by nc_attention_bwd_noalloc_status). */
 nc_status nc_selftest_wait_timeout(int timeout_us, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus

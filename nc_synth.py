@@ -136,3 +136,16 @@ def make_e4m3_codes(rows: int, cols: int, seed: int, exp_lo: int = 3, exp_hi: in
     e = rng.integers(exp_lo, exp_hi + 1, size=(rows, cols), dtype=np.uint8)
     m = rng.integers(0, 8, size=(rows, cols), dtype=np.uint8)
     return (s << 7) | (e << 3) | m
+
+
+def make_e4m3_codes_full(rows: int, cols: int, seed: int):
+    """Random 8-bit codes over the whole code space except the two NaN codes
+    (s.1111.111): zeros of both signs, subnormals (exponent field 0), and the
+    largest magnitudes (s.1111.110) all occur.  Bit fields only."""
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    nan = (c & 0x7F) == 0x7F
+    while nan.any():
+        c[nan] = rng.integers(0, 256, size=int(nan.sum()), dtype=np.uint8)
+        nan = (c & 0x7F) == 0x7F
+    return c

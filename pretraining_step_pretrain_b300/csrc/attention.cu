@@ -208,30 +208,62 @@ cudaError_t attention_bwd(bool bf16, int B, int T, int H, int h, const void* q, 
 // cleared between calls.
 static __device__ __align__(256) float g_noalloc_attn_delta[kNoAllocAttnMaxRows];
 
+// The device error word of the allocation-free calls, laid out like the one
+// at the start of a workspace ([0] status, first writer wins; [1] site; [2]
+// detail).  The kernels' bounded waits record a timeout here; it starts at
+// zero when the library loads and is read and cleared by
+// noalloc_read_status().  Shared by every call, like the array above.
+static __device__ __align__(16) int g_noalloc_err[4];
+
 namespace {
 constexpr int kMaxDevices = 64;
+struct NoAllocPtrs {
+  float* delta = nullptr;
+  int* err = nullptr;
+};
 std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
+NoAllocPtrs g_noalloc_ptr[kMaxDevices];
 }  // namespace
 
-// Device address of the array on the current device.  In host code the name
-// g_noalloc_attn_delta is only a host-side stand-in, never a device address,
-// so it is looked up here once per device (with that device current) and
-// cached.
-static cudaError_t noalloc_delta_ptr(float** out) {
+// Device addresses of the array and the error word on the current device.
+// In host code their names are only host-side stand-ins, never device
+// addresses, so they are looked up here once per device (with that device
+// current) and cached.
+static cudaError_t noalloc_ptrs(NoAllocPtrs* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_attn_delta);
+  NoAllocPtrs& p = g_noalloc_ptr[dev];
+  if (!p.delta) {
+    void* d = nullptr;
+    void* w = nullptr;
+    e = cudaGetSymbolAddress(&d, g_noalloc_attn_delta);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    e = cudaGetSymbolAddress(&w, g_noalloc_err);
+    if (e != cudaSuccess) return e;
+    p.delta = static_cast<float*>(d);
+    p.err = static_cast<int*>(w);
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return cudaSuccess;
+}
+
+cudaError_t noalloc_error_word(int** err) {
+  NoAllocPtrs p;
+  cudaError_t e = noalloc_ptrs(&p);
+  if (e == cudaSuccess) *err = p.err;
+  return e;
+}
+
+cudaError_t noalloc_read_status(cudaStream_t stream, int word[4]) {
+  int* err = nullptr;
+  cudaError_t e = noalloc_error_word(&err);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(word, err, 4 * sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(err, 0, 4 * sizeof(int));
+  return e;
 }
 
 cudaError_t attention_bwd_noalloc(bool bf16, int B, int T, int H, int h, const void* q,
@@ -239,11 +271,13 @@ cudaError_t attention_bwd_noalloc(bool bf16, int B, int T, int H, int h, const v
                                   const void* dout, void* dq, long ldq, void* dk, long ldk,
                                   void* dv, long ldv, const Ctx& ctx) {
   if ((long)B * T * H > kNoAllocAttnMaxRows) return cudaErrorInvalidValue;
-  float* delta = nullptr;
-  cudaError_t e = noalloc_delta_ptr(&delta);
+  NoAllocPtrs p;
+  cudaError_t e = noalloc_ptrs(&p);
   if (e != cudaSuccess) return e;
-  return attention_bwd(bf16, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk, ldk, dv, ldv, delta,
-                       ctx);
+  Ctx c = ctx;
+  c.err = p.err;
+  return attention_bwd(bf16, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk, ldk, dv, ldv,
+                       p.delta, c);
 }
 
 }  // namespace nc

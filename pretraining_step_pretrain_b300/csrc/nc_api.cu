@@ -846,7 +846,7 @@ nc_status nc_attention_bwd_noalloc(int dtype, int B, int T, int H, int h, const 
                 (long)B * T * H, kNoAllocAttnMaxRows);
   Ctx ctx;
   ctx.stream = static_cast<cudaStream_t>(stream);
-  ctx.err = nullptr;  // the attention kernels record no device errors
+  ctx.err = nullptr;  // replaced by the library's own error word of the no-alloc calls
   ctx.timeout_ns = kWaitTimeoutNs;
   ctx.num_sms = sm_count();
   cudaError_t e = attention_bwd_noalloc(dtype == NC_BF16, B, T, H, h, q, k, v, o, lse, dout, dq,
@@ -856,10 +856,24 @@ nc_status nc_attention_bwd_noalloc(int dtype, int B, int T, int H, int h, const 
   return NC_OK;
 }
 
+nc_status nc_attention_bwd_noalloc_status(void* stream) {
+  int word[4] = {0, 0, 0, 0};
+  cudaError_t e = noalloc_read_status(static_cast<cudaStream_t>(stream), word);
+  if (e != cudaSuccess)
+    return fail(NC_ERR_CUDA, "reading the no-alloc error word: %s", cudaGetErrorString(e));
+  if (word[0] == NC_OK) return NC_OK;
+  return fail(static_cast<nc_status>(word[0]), "device reported %s at site %d (detail %d)",
+              nc_status_string(static_cast<nc_status>(word[0])), word[1], word[2]);
+}
+
 nc_status nc_selftest_wait_timeout(int timeout_us, void* ws, size_t ws_bytes, void* stream) {
-  if (!ws || ws_bytes < 16 || timeout_us < 1 || timeout_us > 10000000)
+  if ((ws && ws_bytes < 16) || timeout_us < 1 || timeout_us > 10000000)
     return fail(NC_ERR_INVALID_ARG, "bad selftest arguments");
-  const Ctx ctx = make_ctx(ws, stream, (long long)timeout_us * 1000);
+  Ctx ctx = make_ctx(ws, stream, (long long)timeout_us * 1000);
+  if (!ws) {
+    cudaError_t e = noalloc_error_word(&ctx.err);
+    if (e != cudaSuccess) return fail(NC_ERR_CUDA, "no-alloc error word: %s", cudaGetErrorString(e));
+  }
   cudaError_t e = selftest_wait(ctx.timeout_ns, ctx);
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
   return NC_OK;

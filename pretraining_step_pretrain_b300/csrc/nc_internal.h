@@ -110,6 +110,11 @@ cudaError_t attention_bwd_noalloc(bool bf16, int B, int T, int H, int h, const v
                                   const void* k, const void* v, const void* o, const float* lse,
                                   const void* dout, void* dq, long ldq, void* dk, long ldk,
                                   void* dv, long ldv, const Ctx& ctx);
+// The allocation-free calls' device error word (a fixed device array of the
+// library, like their scratch): its address on the current device, and a
+// synchronising read that clears it.
+cudaError_t noalloc_error_word(int** err);
+cudaError_t noalloc_read_status(cudaStream_t stream, int word[4]);
 
 // ---- loss ----
 cudaError_t softcap_rows_f32(float* s, const int* targets, float* lse, float* s_tgt, int M,

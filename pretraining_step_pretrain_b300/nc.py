@@ -26,7 +26,7 @@ EXPORTS = ("nc_workspace_bytes", "nc_embed_norm", "nc_block_fwd", "nc_lmhead_sof
            "nc_block_bwd", "nc_embed_norm_bwd", "nc_step", "nc_get_device_status",
            "nc_status_string", "nc_last_error_message", "nc_gemm_workspace_bytes", "nc_gemm",
            "nc_attention_workspace_bytes", "nc_attention_fwd", "nc_attention_bwd",
-           "nc_attention_bwd_noalloc",
+           "nc_attention_bwd_noalloc", "nc_attention_bwd_noalloc_status",
            "nc_launch_count", "nc_profile_start", "nc_profile_stop", "nc_profile_record",
            "nc_selftest_wait_timeout", "nc_gemm_batched", "nc_optimizer_workspace_bytes",
            "nc_optimizer_step", "nc_eval", "nc_gemm_fp8")
@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
             "nc_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P, I, P, I, P, I, P, S, P]),
             "nc_attention_bwd_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, I, P, I, P, I,
                                              P]),
+            "nc_attention_bwd_noalloc_status": (I, [P]),
             "nc_selftest_wait_timeout": (I, [I, P, S, P]),
             "nc_launch_count": (ctypes.c_longlong, []),
             "nc_profile_start": (I, [I]),
@@ -279,6 +280,12 @@ def attention_bwd_noalloc(dtype, B, T, H, h, q, k, v, o, lse, dout, dq, ldq, dk,
                                           _ptr(dv), ldv, _stream()))
 
 
+def attention_bwd_noalloc_status() -> int:
+    """Read and clear the device error word of the allocation-free calls
+    (synchronises the current stream); returns the nc_status value."""
+    return lib().nc_attention_bwd_noalloc_status(_stream())
+
+
 def launch_count() -> int:
     return lib().nc_launch_count()
 
@@ -300,7 +307,8 @@ def profile_stop() -> list[tuple[str, float]]:
 
 
 def selftest_wait_timeout(timeout_us: int, ws) -> None:
-    p, n = _ws(ws)
+    """ws None: record into the allocation-free calls' error word."""
+    p, n = _ws(ws) if ws is not None else (None, 0)
     _check(lib().nc_selftest_wait_timeout(timeout_us, p, n, _stream()))
 
 

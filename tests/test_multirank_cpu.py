@@ -68,3 +68,38 @@ def test_two_ranks_shard_time_and_throughput():
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(7.5, 1) == 7.5
     assert bench.job_tokens_per_s(2, 64, 1, 4, 0.5) == 2 * 64 * 4 / 0.5
+
+
+def _bench_cmd(*args):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    return [sys.executable, os.path.join(root, "bench.py"), *args], env
+
+
+def test_bench_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` with no launcher starts two ranks itself (gloo here,
+    host only: --launcher-check runs no GPU work) and reports n_gpus 2."""
+    import json
+    import subprocess
+    cmd, env = _bench_cmd("--gpus", "2", "--launcher-check")
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = lines[0]
+    assert out["n_gpus"] == 2
+    assert sorted(x["rank"] for x in out["ranks"]) == [0, 1]
+    assert all(x["world"] == 2 for x in out["ranks"])
+    assert sorted(x["local_rank"] for x in out["ranks"]) == [0, 1]
+
+
+def test_bench_refuses_a_launcher_world_that_differs_from_gpus():
+    import subprocess
+    cmd, env = _bench_cmd("--gpus", "4", "--launcher-check")
+    env.update(RANK="0", WORLD_SIZE="2", LOCAL_RANK="0")
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2
+    assert "--gpus 4" in r.stderr

@@ -215,30 +215,36 @@ def host_cpu():
     return {"model": model, "nproc": os.cpu_count() or 1}
 
 
-def oracle_tokens_per_s(shape, B, T, min_seconds, max_steps, weights=None, threads=None):
-    """Time the fp64 oracle's full step on B rows of T tokens at `shape` (host
-    cores; `threads` caps the BLAS threads, None leaves them all)."""
-    import contextlib
-
+def oracle_tokens_per_s(shape, B, T, min_seconds, max_steps, weights=None):
+    """Time the fp64 oracle's full step on B rows of T tokens at `shape` on the
+    host cores (as many BLAS threads as the environment gives it)."""
     import oracle
     if weights is None:
         weights = nc_synth.make_weights(shape, seed=1, bf16=True)
     P = {k: v.astype(np.float64) for k, v in weights.items()}
     ids, tg = nc_synth.make_tokens(shape.vocab, B, T, seed=0)
-    limit = contextlib.nullcontext()
-    if threads is not None:
-        from threadpoolctl import threadpool_limits
-        limit = threadpool_limits(threads)
-    with limit:
-        used = blas_threads()
-        oracle.step(shape, P, ids, tg)                   # first touch of every buffer
-        times = []
-        t_all = time.perf_counter()
-        while len(times) < max_steps and (time.perf_counter() - t_all < min_seconds or not times):
-            t0 = time.perf_counter()
-            oracle.step(shape, P, ids, tg)
-            times.append(time.perf_counter() - t0)
-    return B * T * len(times) / sum(times), used, len(times)
+    oracle.step(shape, P, ids, tg)                       # first touch of every buffer
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and (time.perf_counter() - t_all < min_seconds or not times):
+        t0 = time.perf_counter()
+        oracle.step(shape, P, ids, tg)
+        times.append(time.perf_counter() - t0)
+    return B * T * len(times) / sum(times), blas_threads(), len(times)
+
+
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def oracle_one_thread(workload, tokens):
+    """The same oracle timing in a child process whose BLAS runs one thread
+    (the thread count is fixed when the BLAS library loads)."""
+    env = dict(os.environ, **{k: "1" for k in ONE_THREAD_ENV})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", workload,
+                        str(tokens)], env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_baseline(w, weights, tokens, full_d20=False):
@@ -247,12 +253,11 @@ def cpu_baseline(w, weights, tokens, full_d20=False):
     small configurations' full steps, and optionally one whole 2048-token row
     at the depth-20 widths."""
     v, threads, n = oracle_tokens_per_s(w.shape, 1, tokens, 5.0, 2, weights)
-    v1, _, n1 = oracle_tokens_per_s(w.shape, 1, tokens, 0.0, 1, weights, threads=1)
     out = {"value": v, "unit": "tokens/s", "cores": threads, "host": host_cpu(),
            "kind": "oracle",
            "sample": f"{w.name} widths, 1 row x {tokens} tokens, {n} timed full oracle "
                      f"step(s) (forward + backward, fp64) after one untimed",
-           "one_thread": {"value": v1, "unit": "tokens/s", "steps": n1},
+           "one_thread": oracle_one_thread(w.name, tokens),
            "full_steps": {}}
     for name in ("tiny_f32", "small_bf16"):
         o = nc_synth.WORKLOADS[name]
@@ -556,7 +561,14 @@ def main(argv=None):
     ap.add_argument("--no-optimizer", action="store_true")
     ap.add_argument("--launcher-check", action="store_true",
                     help="start the ranks, report the rank layout, run nothing on a GPU")
+    ap.add_argument("--oracle-sample", nargs=2, metavar=("WORKLOAD", "TOKENS"),
+                    help="time the oracle alone on 1 row of TOKENS tokens and print it")
     args = ap.parse_args(argv)
+    if args.oracle_sample:
+        w = nc_synth.WORKLOADS[args.oracle_sample[0]]
+        v, threads, n = oracle_tokens_per_s(w.shape, 1, int(args.oracle_sample[1]), 0.0, 1)
+        print(json.dumps({"value": v, "unit": "tokens/s", "cores": threads, "steps": n}))
+        return
     if args.gpus < 1:
         ap.error("--gpus must be >= 1")
     if "WORLD_SIZE" not in os.environ and args.gpus > 1:

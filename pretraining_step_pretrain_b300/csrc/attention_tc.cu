@@ -397,15 +397,23 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
 }
 
 // ======================================================================
-// backward, dQ pass: 128 packed query rows per CTA against 128-key tiles.
-// Also writes delta = rowsum(dO * O) for the dK/dV pass.  Q and dO, the same
-// for every key tile, sit in tensor memory as the A operands of S = Q K^T
-// and dP = dO V^T, so shared memory only streams K and V.  S and dP (128
-// columns each) are single-buffered: the softmax warps copy them to
-// registers and release them at once, so the next tile's MMAs start while
-// dS is being formed.  Every MMA is N = 128 wide (narrower ones run at
-// ~60% of the tensor rate: their shared-memory operand traffic per FLOP is
-// higher).
+// backward, dQ pass: persistent CTAs, one per SM, each walking a list of
+// 128-row query tiles (heaviest first, the order reversed every other round
+// so that every CTA gets a similar share of key tiles).  Per query tile the
+// CTA streams the key tiles it sees; Q and dO of the tile stay in shared
+// memory as the A operands of S = Q K^T and dP = dO V^T while K and V stream
+// through rings of their own (K, read by the S and dQ products, three stages;
+// V, read only by dP and so released earlier, two), so the loads of the next
+// key tiles are in flight while the current ones are used; dQ accumulates in
+// tensor memory.  One counter
+// g runs over every (query tile, key tile) pair of the CTA, so the rings,
+// buffers and barrier phases carry on across query tiles: the MMA thread
+// issues S/dP of the next pair (the next query tile's first one included)
+// before the dQ product of the current one, and the softmax warps drain a
+// finished dQ while the tensor pipe already computes the next tile's scores.
+// The next tile's Q and dO are prefetched into L2 while the current tile
+// runs and loaded once the last S/dP of the current tile are done.  Every
+// MMA is N = 128 wide (narrower ones run at ~60% of the tensor rate).
 // ======================================================================
 // delta[r] = sum_d O[r][d] dO[r][d] in fp32 for every packed row r (the
 // softmax-gradient row term of the attention backward): 16 threads per row,
@@ -436,60 +444,91 @@ __global__ void __launch_bounds__(256)
 namespace bdq {
 constexpr int BQ = 128, BKV = 128;
 constexpr int ATOM = 16384;                  // [128 rows][64] bf16
-constexpr int KVS = 2;                       // K/V ring stages (64 KB each)
-constexpr int K_OFF = 0;                     // KVS x 32 KB ([128 keys][128 dims] = 2 atoms)
-constexpr int V_OFF = K_OFF + KVS * 32768;   // KVS x 32 KB
-constexpr int Q_OFF = V_OFF + KVS * 32768;   // 32 KB, the CTA's 128 rows
+constexpr int KS = 3;                        // K ring stages (32 KB each): K is read by S and dQ
+constexpr int VS = 2;                        // V ring stages (32 KB each): V only by dP
+constexpr int K_OFF = 0;                     // KS x 32 KB ([128 keys][128 dims] = 2 atoms)
+constexpr int V_OFF = K_OFF + KS * 32768;    // VS x 32 KB
+constexpr int Q_OFF = V_OFF + VS * 32768;    // 32 KB, the current tile's 128 rows
 constexpr int DO_OFF = Q_OFF + 32768;        // 32 KB
 constexpr int BAR_OFF = DO_OFF + 32768;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
+constexpr int kPrefetchAhead = 4;            // key tiles prefetched into L2 ahead of their load
 static_assert(SMEM <= 232448, "dQ pass shared memory exceeds 227 KB");
 }  // namespace bdq
+
+// The k-th query tile (an index into the heaviest-first order: sequence
+// fastest, the last query tiles -- which see the most keys -- first) of CTA c
+// among G, or -1 past the end.  Round k covers tiles kG .. kG + G - 1, walked
+// forwards in even rounds and backwards in odd ones.
+__device__ __forceinline__ long dq_tile_of(int c, int k, int G, long n_tiles) {
+  const long u = (long)k * G + ((k & 1) ? G - 1 - c : c);
+  return u < n_tiles ? u : -1;
+}
 
 __global__ void __launch_bounds__(NT, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmDO, const float* __restrict__ lse,
-                          const float* __restrict__ delta, bf16* __restrict__ dq, long ldq, int T,
-                          int H, int* err, long long timeout_ns) {
+                          const float* __restrict__ delta, bf16* __restrict__ dq, long ldq, int B,
+                          int T, int H, int* err, long long timeout_ns) {
   using namespace bdq;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* kv_full = bars + 1;         // [KVS] (bars + 0 is unused)
-  uint64_t* kv_empty = bars + 1 + KVS;  // [KVS]
-  uint64_t* s_full = bars + 1 + 2 * KVS;    // S and dP of the tile ready
-  uint64_t* s_free = bars + 2 + 2 * KVS;    // copied out, one arrival per softmax warp
-  uint64_t* ds_full = bars + 3 + 2 * KVS;   // [2] by dS buffer, one arrival per softmax warp
-  uint64_t* dq_done = bars + 5 + 2 * KVS;   // [2] by dS buffer: the dQ MMA that read it is done
-  uint64_t* drain = bars + 7 + 2 * KVS;
-  uint64_t* qd_full = bars + 8 + 2 * KVS;   // Q and dO tiles staged (TMA)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9 + 2 * KVS);
+  uint64_t* k_full = bars + 0;              // [KS]
+  uint64_t* k_empty = bars + KS;            // [KS]: the dQ product read it
+  uint64_t* v_full = bars + 2 * KS;         // [VS]
+  uint64_t* v_empty = bars + 2 * KS + VS;   // [VS]: the dP product read it
+  uint64_t* s_full = bars + 2 * (KS + VS);      // S of the pair ready
+  uint64_t* s_free = s_full + 1;            // S copied out, one arrival per softmax warp
+  uint64_t* ds_full = s_full + 2;           // [2] by dS buffer, one arrival per softmax warp
+  uint64_t* dq_done = s_full + 4;           // [2] by dS buffer: the dQ MMA that read it is done
+  uint64_t* drain = s_full + 6;             // [2], one per MMA issuer
+  uint64_t* qd_full = s_full + 8;           // the tile's Q and dO staged (TMA)
+  uint64_t* qd_free = s_full + 9;           // the tile's last S / dP products are done
+  uint64_t* dq_full = s_full + 10;          // the tile's last dQ product is done
+  uint64_t* dp_full = s_full + 11;          // dP of the pair ready
+  uint64_t* dp_free = s_full + 12;          // dP copied out, one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
   const long TH = (long)T * H;
   const int n_qt = (int)((TH + BQ - 1) / BQ);
-  const long r0 = (long)(n_qt - 1 - blockIdx.y) * BQ;
-  const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
-  const int nkv = t_last / BKV + 1;
+  const long n_tiles = (long)B * n_qt;
+  const int G = gridDim.x, c = blockIdx.x;
+  // tile u -> sequence b, first packed row r0, key tiles nkv
+  auto tile_b = [&](long u) { return (int)(u % B); };
+  auto tile_r0 = [&](long u) { return (long)(n_qt - 1 - (int)(u / B)) * BQ; };
+  auto tile_nkv = [&](long u) {
+    const long r0 = tile_r0(u);
+    return (int)(min(r0 + BQ - 1, TH - 1) / H) / BKV + 1;
+  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < KVS; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < KS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < VS; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, NSW);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, NSW);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ds_full[i], NSW);
       mbar_init(&dq_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(qd_full, 1);
+    mbar_init(qd_free, 1);
+    mbar_init(dq_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -503,90 +542,156 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = *tmem_slot;
   const CtaSync sync{abort_flag, err, timeout_ns};
   // TMEM columns: S at 0, dP at 128, dQ at 256, dS at 384 and 448 (bf16 pairs,
-  // by tile parity).
+  // by the parity of the pair counter g).
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer (Q, dO; K, V)
-    mbar_arrive_expect_tx(qd_full, 4 * ATOM);
-    tma_load_3d(smem + Q_OFF, &tmQ, qd_full, 0, (int)r0, b);
-    tma_load_3d(smem + Q_OFF + ATOM, &tmQ, qd_full, 64, (int)r0, b);
-    tma_load_3d(smem + DO_OFF, &tmDO, qd_full, 0, (int)r0, b);
-    tma_load_3d(smem + DO_OFF + ATOM, &tmDO, qd_full, 64, (int)r0, b);
-    int armed[KVS];
-    for (int i = 0; i < KVS; ++i) armed[i] = -1;
-    for (int j = 0; j < nkv; ++j) {
-      const int ks = j % KVS;
-      const uint32_t kph = (j / KVS) & 1;
-      if (!sync.wait(&kv_empty[ks], kph ^ 1u)) break;
-      mbar_arrive_expect_tx(&kv_full[ks], 4 * ATOM);
-      tma_load_3d(smem + K_OFF + ks * 32768, &tmK, &kv_full[ks], 0, j * BKV, b);
-      tma_load_3d(smem + K_OFF + ks * 32768 + ATOM, &tmK, &kv_full[ks], 64, j * BKV, b);
-      tma_load_3d(smem + V_OFF + ks * 32768, &tmV, &kv_full[ks], 0, j * BKV, b);
-      tma_load_3d(smem + V_OFF + ks * 32768 + ATOM, &tmV, &kv_full[ks], 64, j * BKV, b);
-      armed[ks] = (int)kph;
+    // ------------------------------------------------ TMA producer (Q, dO per tile; K, V rings)
+    int armed_qd = -1;
+    int armed_k[KS], armed_v[VS];
+    for (int i = 0; i < KS; ++i) armed_k[i] = -1;
+    for (int i = 0; i < VS; ++i) armed_v[i] = -1;
+    long g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const long u = dq_tile_of(c, k, G, n_tiles);
+      if (u < 0) break;
+      const int b = tile_b(u);
+      const int r0 = (int)tile_r0(u);
+      if (k > 0 && !sync.wait(qd_free, (k - 1) & 1)) break;
+      mbar_arrive_expect_tx(qd_full, 4 * ATOM);
+      tma_load_3d(smem + Q_OFF, &tmQ, qd_full, 0, r0, b);
+      tma_load_3d(smem + Q_OFF + ATOM, &tmQ, qd_full, 64, r0, b);
+      tma_load_3d(smem + DO_OFF, &tmDO, qd_full, 0, r0, b);
+      tma_load_3d(smem + DO_OFF + ATOM, &tmDO, qd_full, 64, r0, b);
+      armed_qd = k & 1;
+      const long un = dq_tile_of(c, k + 1, G, n_tiles);
+      if (un >= 0) {  // the next tile's rows into L2 while this one runs
+        const int bn = tile_b(un), rn = (int)tile_r0(un);
+        tma_prefetch_l2_3d(&tmQ, 0, rn, bn);
+        tma_prefetch_l2_3d(&tmQ, 64, rn, bn);
+        tma_prefetch_l2_3d(&tmDO, 0, rn, bn);
+        tma_prefetch_l2_3d(&tmDO, 64, rn, bn);
+      }
+      const int nkv = tile_nkv(u);
+      for (int j = 0; j < nkv; ++j, ++g) {
+        if (j + kPrefetchAhead < nkv) {  // key tiles a few pairs ahead into L2
+          tma_prefetch_l2_3d(&tmK, 0, (j + kPrefetchAhead) * BKV, b);
+          tma_prefetch_l2_3d(&tmK, 64, (j + kPrefetchAhead) * BKV, b);
+          tma_prefetch_l2_3d(&tmV, 0, (j + kPrefetchAhead) * BKV, b);
+          tma_prefetch_l2_3d(&tmV, 64, (j + kPrefetchAhead) * BKV, b);
+        }
+        const int ks = (int)(g % KS), vs = (int)(g % VS);
+        const uint32_t kph = (uint32_t)(g / KS) & 1u, vph = (uint32_t)(g / VS) & 1u;
+        if (!sync.wait(&v_empty[vs], vph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[vs], 2 * ATOM);
+        tma_load_3d(smem + V_OFF + vs * 32768, &tmV, &v_full[vs], 0, j * BKV, b);
+        tma_load_3d(smem + V_OFF + vs * 32768 + ATOM, &tmV, &v_full[vs], 64, j * BKV, b);
+        armed_v[vs] = (int)vph;
+        if (!sync.wait(&k_empty[ks], kph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[ks], 2 * ATOM);
+        tma_load_3d(smem + K_OFF + ks * 32768, &tmK, &k_full[ks], 0, j * BKV, b);
+        tma_load_3d(smem + K_OFF + ks * 32768 + ATOM, &tmK, &k_full[ks], 64, j * BKV, b);
+        armed_k[ks] = (int)kph;
+      }
     }
     if (*abort_flag) {
       int none = 0;
-      mbar_wait_bounded(qd_full, 0, &none, err, SITE_ATTN, timeout_ns / 8);
-      for (int i = 0; i < KVS; ++i)
-        if (armed[i] >= 0)
-          mbar_wait_bounded(&kv_full[i], (uint32_t)armed[i], &none, err, SITE_ATTN,
+      if (armed_qd >= 0)
+        mbar_wait_bounded(qd_full, (uint32_t)armed_qd, &none, err, SITE_ATTN, timeout_ns / 8);
+      for (int i = 0; i < KS; ++i)
+        if (armed_k[i] >= 0)
+          mbar_wait_bounded(&k_full[i], (uint32_t)armed_k[i], &none, err, SITE_ATTN,
+                            timeout_ns / 8);
+      for (int i = 0; i < VS; ++i)
+        if (armed_v[i] >= 0)
+          mbar_wait_bounded(&v_full[i], (uint32_t)armed_v[i], &none, err, SITE_ATTN,
                             timeout_ns / 8);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer
-    // Kept lean (see the dK/dV pass): descriptors are built once and a k-step
-    // or ring stage only moves the start-address field.
+  } else if ((warp == 1 || warp == 3) && lane == 0) {
+    // ------------------------------------------------ MMA issuers
+    // Two threads issue the MMAs: warp 1 the S = Q K^T and dP = dO V^T
+    // products of every pair, warp 3 the dQ += dS K products.  An MMA issue
+    // holds its thread for about the MMA's run time, so with one issuer every
+    // barrier wait and commit between two MMA groups left the tensor pipe
+    // idle; with two, one stream's bookkeeping overlaps the other's MMAs.  A
+    // commit tracks the MMAs of its own thread, which is exactly what each
+    // release needs (K of pair g is last read by dQ(g), which follows S(g)
+    // through the softmax warps' dS).  Descriptors are built once; a k-step or
+    // ring stage only moves the start-address field.
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idQ = idesc_bf16_mn(false, true, BQ, HD);
     constexpr uint64_t kStage = 32768 >> 4;
-    const uint64_t dKk = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);    // K-major
-    const uint64_t dKm = sdesc_sw128(smem_u32(smem + K_OFF), ATOM, 1024);  // MN-major
-    const uint64_t dVk = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
-    const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
-    const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
     auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
     auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
-    bool ok = sync.wait(qd_full, 0), issued = false;
-    // S(j) and dP(j) into their TMEM buffers once tile j - 1's copies are out.
-    auto issue_s = [&](int j) -> bool {
-      const int ks = j % KVS;
-      if (!sync.wait(&kv_full[ks], (j / KVS) & 1)) return false;
-      if (j > 0 && !sync.wait(s_free, (j - 1) & 1)) return false;
-      tc_fence_after();
-      const uint64_t bk = dKk + ks * kStage, bv = dVk + ks * kStage;
+    bool ok = true, issued = false;
+    long g = 0;
+    if (warp == 1) {
+      const uint64_t dKk = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);    // K-major
+      const uint64_t dVk = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
+      const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
+      for (int k = 0; ok; ++k) {
+        const long u = dq_tile_of(c, k, G, n_tiles);
+        if (u < 0) break;
+        const int nkv = tile_nkv(u);
+        if (!sync.wait(qd_full, (uint32_t)k & 1u)) { ok = false; break; }
+        for (int j = 0; j < nkv; ++j, ++g) {
+          // S(g), then dP(g), each into its TMEM buffer once pair g - 1's copy
+          // of it is out: the softmax warps start on S(g) while dP(g) runs.
+          const int ks = (int)(g % KS), vs = (int)(g % VS);
+          if (!sync.wait(&k_full[ks], (uint32_t)(g / KS) & 1u) ||
+              (g > 0 && !sync.wait(s_free, (uint32_t)(g - 1) & 1u))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bk = dKk + ks * kStage, bv = dVk + vs * kStage;
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        umma_bf16(tmem + 0, dQk + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
-        umma_bf16(tmem + 128, dOk + koff(kk), bv + koff(kk), idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + 0, dQk + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
+          umma_commit(s_full);
+          if (!sync.wait(&v_full[vs], (uint32_t)(g / VS) & 1u) ||
+              (g > 0 && !sync.wait(dp_free, (uint32_t)(g - 1) & 1u))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + 128, dOk + koff(kk), bv + koff(kk), idS, kk > 0 ? 1u : 0u);
+          umma_commit(dp_full);
+          umma_commit(&v_empty[vs]);
+          if (j == nkv - 1) umma_commit(qd_free);  // the tile's Q, dO are read for the last time
+          issued = true;
+        }
       }
-      umma_commit(s_full);
-      issued = true;
-      return true;
-    };
-    // dQ += dS(j) K(j)
-    auto issue_dq = [&](int j) -> bool {
-      const int ks = j % KVS, db = j & 1;
-      if (!sync.wait(&ds_full[db], (j >> 1) & 1)) return false;
-      tc_fence_after();
-      const uint64_t bk = dKm + ks * kStage;
+    } else {
+      const uint64_t dKm = sdesc_sw128(smem_u32(smem + K_OFF), ATOM, 1024);  // MN-major
+      for (int k = 0; ok; ++k) {
+        const long u = dq_tile_of(c, k, G, n_tiles);
+        if (u < 0) break;
+        const int nkv = tile_nkv(u);
+        for (int j = 0; j < nkv; ++j, ++g) {
+          // dQ (+)= dS(g) K(g), dS(g) read from tensor memory
+          const int ks = (int)(g % KS), db = (int)(g & 1);
+          if (!sync.wait(&ds_full[db], (uint32_t)(g >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bk = dKm + ks * kStage;
 #pragma unroll
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16_tmem_a(tmem + 256, tmem + 384 + db * 64 + kk * 8, bk + moff(kk), idQ,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&dq_done[db]);
-      umma_commit(&kv_empty[ks]);
-      return true;
-    };
-    if (ok) ok = issue_s(0);
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-      if (!issue_dq(j)) { ok = false; break; }
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            umma_bf16_tmem_a(tmem + 256, tmem + 384 + db * 64 + kk * 8, bk + moff(kk), idQ,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&dq_done[db]);
+          umma_commit(&k_empty[ks]);
+          if (j == nkv - 1) umma_commit(dq_full);
+          issued = true;
+        }
+      }
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      umma_commit(&drain[warp == 1 ? 0 : 1]);
+      mbar_wait_bounded(&drain[warp == 1 ? 0 : 1], 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax warps
@@ -595,67 +700,111 @@ __global__ void __launch_bounds__(NT, 1)
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
-    const long r = r0 + row;
-    const bool valid = r < TH;
-    const int t = (int)(r / H);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
-    const long grow = (long)b * TH + r;
-    const float dl = valid ? delta[grow] : 0.f;
-    const float lse2 = valid ? lse[grow] * kLog2e : 0.f;
     bool ok = true;
-    // Rows of this CTA hold tokens t0 .. t_last; a key tile needs the mask
-    // only where it reaches past t0 (or the tile has rows past the sequence).
-    const int t0 = (int)(r0 / H);
-    const bool rows_ragged = r0 + BQ > TH;
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (!sync.wait(s_full, j & 1)) { ok = false; break; }
-      tc_fence_after();
-      float s[64], dp[64];
-      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(s));
-      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-      tmem_ld_32cols(tmem + lane_off + 128 + half * 64, *reinterpret_cast<float(*)[32]>(dp));
-      tmem_ld_32cols(tmem + lane_off + 128 + half * 64 + 32,
-                     *reinterpret_cast<float(*)[32]>(dp + 32));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      const int key0 = j * BKV + half * 64;
-      const bool need_mask = rows_ragged || key0 + 63 > t0;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) s[i] = ex2(fmaf(s[i], sl2, -lse2));
-      if (need_mask) {  // key key0 + i is visible to token t; padding rows see nothing
-        const int lim = valid ? t - key0 : -1;
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i > lim) s[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 64; i += 2) sub_mul2(s[i], s[i + 1], dp[i], dp[i + 1], dl, dl, s[i], s[i + 1]);
-      const int db = j & 1;
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack2(s[2 * i], s[2 * i + 1]);
-      if (j > 1) {  // the dQ MMA of tile j - 2 has read this dS buffer
-        if (!sync.wait(&dq_done[db], ((j >> 1) - 1) & 1)) { ok = false; break; }
+    long g = 0;
+    // this row's lse and delta, one tile ahead
+    auto row_data = [&](long u, float& l2, float& d) {
+      const long r = tile_r0(u) + row;
+      const bool v = r < TH;
+      const long grow = (long)tile_b(u) * TH + r;
+      d = v ? delta[grow] : 0.f;
+      l2 = v ? lse[grow] * kLog2e : 0.f;
+    };
+    long u = dq_tile_of(c, 0, G, n_tiles);
+    float lse2 = 0.f, dl = 0.f;
+    if (u >= 0) row_data(u, lse2, dl);
+    for (int k = 0; ok && u >= 0; ++k) {
+      const int b = tile_b(u);
+      const long r0 = tile_r0(u);
+      const long r = r0 + row;
+      const bool valid = r < TH;
+      const int t = (int)(r / H);
+      const int nkv = tile_nkv(u);
+      const long un = dq_tile_of(c, k + 1, G, n_tiles);
+      float lse2_n = 0.f, dl_n = 0.f;
+      if (un >= 0) row_data(un, lse2_n, dl_n);
+      // Rows of this tile hold tokens t0 .. ; a key tile needs the mask only
+      // where it reaches past t0 (or the tile has rows past the sequence).
+      const int t0 = (int)(r0 / H);
+      const bool rows_ragged = r0 + BQ > TH;
+      for (int j = 0; j < nkv; ++j, ++g) {
+        if (!sync.wait(s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
+        float s[64], dp[64];
+        {
+          uint32_t r0_[32], r1_[32];
+          tmem_ld_32cols_nowait(tmem + lane_off + half * 64, r0_);
+          tmem_ld_32cols_nowait(tmem + lane_off + half * 64 + 32, r1_);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(r0_[i]);
+            s[32 + i] = __uint_as_float(r1_[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        const int key0 = j * BKV + half * 64;
+        const bool need_mask = rows_ragged || key0 + 63 > t0;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] = ex2(fmaf(s[i], sl2, -lse2));
+        if (need_mask) {  // key key0 + i is visible to token t; padding rows see nothing
+          const int lim = valid ? t - key0 : -1;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i > lim) s[i] = 0.f;
+        }
+        if (!sync.wait(dp_full, (uint32_t)g & 1u)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t r2_[32], r3_[32];
+          tmem_ld_32cols_nowait(tmem + lane_off + 128 + half * 64, r2_);
+          tmem_ld_32cols_nowait(tmem + lane_off + 128 + half * 64 + 32, r3_);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            dp[i] = __uint_as_float(r2_[i]);
+            dp[32 + i] = __uint_as_float(r3_[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dp_free);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2)
+          sub_mul2(s[i], s[i + 1], dp[i], dp[i + 1], dl, dl, s[i], s[i + 1]);
+        const int db = (int)(g & 1);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack2(s[2 * i], s[2 * i + 1]);
+        if (g > 1) {  // the dQ MMA of pair g - 2 has read this dS buffer
+          if (!sync.wait(&dq_done[db], (uint32_t)((g >> 1) - 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+        }
+        pairs_to_tmem(tmem + lane_off + 384 + db * 64 + half * 32, pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full[db]);
       }
-      pairs_to_tmem(tmem + lane_off + 384 + db * 64 + half * 32, pk);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ds_full[db]);
-    }
-    // dQ MMAs complete in issue order: the last one done means all are.
-    if (ok && sync.wait(&dq_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1)) {
+      if (!ok) break;
+      // dQ MMAs complete in issue order: the tile's last one done means all are.
+      if (!sync.wait(dq_full, (uint32_t)k & 1u)) { ok = false; break; }
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       bf16* qrow = dq + ((long)b * T + t) * ldq + (long)(r % H) * HD;
 #pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+      for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
         float v[32];
-        tmem_ld_32cols(tmem + lane_off + 256 + c * 32, v);
-        if (valid) store_bf16_32(qrow + c * 32, v, scale);
+        tmem_ld_32cols(tmem + lane_off + 256 + cc * 32, v);
+        if (valid) store_bf16_32(qrow + cc * 32, v, scale);
       }
+      tc_fence_before();
+      u = un;
+      lse2 = lse2_n;
+      dl = dl_n;
     }
   }
   tc_fence_before();
@@ -943,8 +1092,17 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc_fence_after();
       float x[64];
-      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(x));
-      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      {
+        uint32_t r0_[32], r1_[32];
+        tmem_ld_32cols_nowait(tmem + lane_off + half * 64, r0_);
+        tmem_ld_32cols_nowait(tmem + lane_off + half * 64 + 32, r1_);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0_[c]);
+          x[32 + c] = __uint_as_float(r1_[c]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sc_free);
@@ -978,8 +1136,17 @@ __global__ void __launch_bounds__(NT, 1)
       // dS^T = P^T (dP^T - delta), with P^T as stored (bf16)
       if (!sync.wait(sc_full, 1)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld_32cols(tmem + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(x));
-      tmem_ld_32cols(tmem + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+      {
+        uint32_t r0_[32], r1_[32];
+        tmem_ld_32cols_nowait(tmem + lane_off + half * 64, r0_);
+        tmem_ld_32cols_nowait(tmem + lane_off + half * 64 + 32, r1_);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0_[c]);
+          x[32 + c] = __uint_as_float(r1_[c]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sc_free);
@@ -1085,9 +1252,10 @@ cudaError_t attention_bwd_tc(int B, int T, int H, const void* q, const void* k, 
   note_launch(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 gq(B, (unsigned)((TH + bdq::BQ - 1) / bdq::BQ));
+  const long dq_tiles = (long)B * ((TH + bdq::BQ - 1) / bdq::BQ);
+  const unsigned gq = (unsigned)std::min<long>(dq_tiles, std::max(ctx.num_sms, 1));
   attn_bwd_dq_tc_kernel<<<gq, NT, bdq::SMEM, ctx.stream>>>(
-      mk, mv, mq, mdo, lse, delta, (nc::bf16*)dq, ldq, T, H, ctx.err, ctx.timeout_ns);
+      mk, mv, mq, mdo, lse, delta, (nc::bf16*)dq, ldq, B, T, H, ctx.err, ctx.timeout_ns);
   note_launch(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -88,18 +88,22 @@ def attn(a):
     v = torch.randn(B, T, h, generator=g, device="cuda").to(bf)
     o = torch.empty_like(q)
     lse = torch.empty(B, T, H, device="cuda")
-    ws = None
-    for _ in range(a.iters):
-        ws = nc.attention_fwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse, ws=ws)
+    ws = nc.attention_fwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse)
+    causal = B * H * T * T * h            # one causal-half matmul
+    ms = _timed(lambda: nc.attention_fwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse, ws=ws),
+                a.iters - 1)
+    print(f"attention fwd B={B} T={T} H={H}: ok" + _rate(ms, 2.0 * causal))
     if a.bwd:
         do = torch.randn_like(q, dtype=torch.float32).to(bf)
         W = (H + 2) * h
         dqkv = torch.empty(B * T, W, dtype=bf, device="cuda")
-        for _ in range(a.iters):
+
+        def bwd():
             nc.attention_bwd(nc.NC_BF16, B, T, H, h, q, k, v, o, lse, do, dqkv[:, :H * h], W,
                              dqkv[:, H * h:H * h + h], W, dqkv[:, H * h + h:], W, ws=ws)
-    torch.cuda.synchronize()
-    print(f"attention B={B} T={T} H={H} bwd={a.bwd}: ok")
+        bwd()
+        ms = _timed(bwd, a.iters - 1)
+        print(f"attention bwd B={B} T={T} H={H}: ok" + _rate(ms, 5.0 * causal))
 
 
 def step(a):

@@ -51,9 +51,20 @@ def test_measured_traffic_needs_the_captured_source(tmp_path, monkeypatch):
     assert bench.measured_traffic("bwd.attention") is None
 
 
-def test_committed_traffic_record_matches_current_source():
-    """The recorded attention traffic is valid for the kernels as committed."""
-    assert bench.measured_traffic("bwd.attention") is not None
+def test_committed_traffic_records_follow_their_sources():
+    """Every committed traffic record is reported exactly while its kernel
+    source is unchanged since the capture, and as null afterwards."""
+    with open(bench.TRAFFIC_FILE) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert rows
+    for group, value, sha, *srcs in rows:
+        h = hashlib.sha256()
+        for src in srcs:
+            with open(os.path.join(bench.ROOT, "pretraining_step_pretrain_b300", "csrc", src),
+                      "rb") as g:
+                h.update(g.read())
+        expect = float(value) if h.hexdigest()[:16] == sha else None
+        assert bench.measured_traffic(group) == expect, group
 
 
 def test_load_peaks_measured_or_fallback(tmp_path, monkeypatch):

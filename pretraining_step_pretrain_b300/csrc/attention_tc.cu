@@ -8,8 +8,11 @@
 // packed rows meets a single K/V tile and every K/V byte brought on chip
 // serves all H heads; key j is visible to packed row r iff j <= r / H.
 //
-// Every kernel is warp-specialised: warp 0 issues TMA, warp 1 issues
-// tcgen05.mma, warp 2 owns the TMEM allocation, and the warps from 4 on are
+// Every kernel is warp-specialised: warp 0 issues TMA, two single threads
+// issue tcgen05.mma (one for the score products, one for the products that
+// consume the softmax warps' output: an MMA issue holds its thread for about
+// the MMA's run time, so a lone issuer's waits and commits would idle the
+// tensor pipe), warp 2 owns the TMEM allocation, and the warps from 4 on are
 // softmax warpgroups -- a thread owns one TMEM lane, i.e. one row of the
 // score tile, and a slice of its columns (the slices of a row belong to the
 // threads of the same lane in the other warpgroups): two warpgroups of 64
@@ -156,10 +159,10 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
   uint64_t* s_free = bars + 11;  // [2], one arrival per softmax warp
   uint64_t* p_full = bars + 13;   // [2] by P buffer, one arrival per softmax warp
   uint64_t* pv_done = bars + 15;  // [2] by P buffer: the PV MMA that read it is done
-  uint64_t* drain = bars + 17;
-  uint64_t* red_full = bars + 18;  // [2], one arrival per softmax warp
-  uint64_t* lsum_full = bars + 20; // one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  uint64_t* drain = bars + 17;     // [2], one per MMA issuer
+  uint64_t* red_full = bars + 19;  // [2], one arrival per softmax warp
+  uint64_t* lsum_full = bars + 21; // one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,7 +185,8 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
       mbar_init(&p_full[i], NSWF);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(&red_full[0], NSWF);
     mbar_init(&red_full[1], NSWF);
     mbar_init(lsum_full, NSWF);
@@ -226,53 +230,61 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
       for (int i = 0; i < 5; ++i)
         if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer
-    // Descriptors are built once; a k-step or ring stage only moves the
-    // 14-bit start-address field (shared memory < 256 KB: no carry).
+  } else if ((warp == 1 || warp == 3) && lane == 0) {
+    // ------------------------------------------------ MMA issuers
+    // Warp 1 issues the score products S(j) = Q K(j)^T, warp 3 the O += P(j)
+    // V(j) products.  An MMA issue holds its thread for about the MMA's run
+    // time, so one stream's waits and commits overlap the other's MMAs; a
+    // commit tracks the MMAs of its own thread (K is read only by the S
+    // products, V only by the PV products).  Descriptors are built once; a
+    // k-step or ring stage only moves the 14-bit start-address field (shared
+    // memory < 256 KB: no carry).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idPV = idesc_bf16_mn(false, true, BQ, HD);
     constexpr uint64_t kStage = 32768 >> 4;
-    const uint64_t dQ = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
-    const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), ATOM, 1024);  // MN-major
     auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
     auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
-    bool ok = sync.wait(q_full, 0), issued = false;
-    auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&k_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) return false;
-      tc_fence_after();
-      const uint64_t bk = dK + st * kStage;
+    bool ok = true, issued = false;
+    if (warp == 1) {
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+      ok = sync.wait(q_full, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!sync.wait(&k_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bk = dK + st * kStage;
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + st * BKV, dQ + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
-      umma_commit(&s_full[st]);
-      umma_commit(&k_empty[st]);
-      issued = true;
-      return true;
-    };
-    if (ok) ok = issue_s(0);
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-      // O += P(j) V(j), P(j) read from tensor memory
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&p_full[st], ph) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
-      tc_fence_after();
-      const uint64_t bv = dV + st * kStage;
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + st * BKV, dQ + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_commit(&s_full[st]);
+        umma_commit(&k_empty[st]);
+        issued = true;
+      }
+    } else {
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), ATOM, 1024);  // MN-major
+      for (int j = 0; ok && j < nkv; ++j) {
+        // O += P(j) V(j), P(j) read from tensor memory
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!sync.wait(&p_full[st], ph) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bv = dV + st * kStage;
 #pragma unroll
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16_tmem_a(tmem + 256, tmem + 384 + st * 64 + kk * 8, bv + moff(kk), idPV,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&pv_done[st]);
-      umma_commit(&v_empty[st]);
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          umma_bf16_tmem_a(tmem + 256, tmem + 384 + st * 64 + kk * 8, bv + moff(kk), idPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[st]);
+        umma_commit(&v_empty[st]);
+        issued = true;
+      }
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      uint64_t* d = &drain[warp == 1 ? 0 : 1];
+      umma_commit(d);
+      mbar_wait_bounded(d, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax / epilogue
@@ -405,12 +417,12 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
 // through rings of their own (K, read by the S and dQ products, three stages;
 // V, read only by dP and so released earlier, two), so the loads of the next
 // key tiles are in flight while the current ones are used; dQ accumulates in
-// tensor memory.  One counter
-// g runs over every (query tile, key tile) pair of the CTA, so the rings,
-// buffers and barrier phases carry on across query tiles: the MMA thread
-// issues S/dP of the next pair (the next query tile's first one included)
-// before the dQ product of the current one, and the softmax warps drain a
-// finished dQ while the tensor pipe already computes the next tile's scores.
+// tensor memory.  One counter g runs over every (query tile, key tile) pair
+// of the CTA, so the rings, buffers and barrier phases carry on across query
+// tiles: the score products of the next pair (the next query tile's first
+// one included) are issued while the dQ product of the current one waits for
+// dS, and the softmax warps drain a finished dQ while the tensor pipe already
+// computes the next tile's scores.
 // The next tile's Q and dO are prefetched into L2 while the current tile
 // runs and loaded once the last S/dP of the current tile are done.  Every
 // MMA is N = 128 wide (narrower ones run at ~60% of the tensor rate).
@@ -842,15 +854,13 @@ static_assert(SLACK >= 0, "dK/dV pass shared memory exceeds 227 KB");
 }  // namespace bkv
 
 // dK/dV pass: one CTA per 128-key tile, K and V resident in shared memory,
-// query tiles (Q, dO) streamed through two TMA rings.  Per query tile i the
-// MMA thread issues, in this order,
-//   S^T(i) = K Q(i)^T,  dV += P^T(i-1) dO(i-1),  dP^T(i) = V dO(i)^T,
-//   dK += dS^T(i-1) Q(i-1),
-// so the tensor pipe always has the previous tile's gradient products to run
-// while the softmax warps turn S^T(i) into P^T(i) and dP^T(i) into dS^T(i).
-// S^T and dP^T share one 128-column score buffer; the softmax warps write
-// P^T and dS^T as bf16 into tensor memory, where the dV and dK products read
-// them as their A operand.  Shared-memory traffic per query tile is then the
+// query tiles (Q, dO) streamed through two TMA rings.  Per query tile i one
+// MMA thread issues S^T(i) = K Q(i)^T and dP^T(i) = V dO(i)^T, another
+// dV += P^T(i) dO(i) and dK += dS^T(i) Q(i), so the gradient products of
+// one tile run while the score products of the next wait for the softmax
+// warps.  S^T and dP^T share one 128-column score buffer; the softmax warps
+// write P^T and dS^T as bf16 into tensor memory, where the dV and dK
+// products read them as their A operand.  Shared-memory traffic per query tile is then the
 // TMA fills (64 KB) and the B operands plus K, V (192 KB): below the tensor
 // pipe's time for the four 128 x 128 x 128 products.
 __global__ void __launch_bounds__(NT, 1)
@@ -879,12 +889,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* sc_free = bars + 12;     // copied out, one arrival per softmax warp
   uint64_t* p_full = bars + 13;      // P^T stored, one arrival per softmax warp
   uint64_t* ds_full = bars + 14;     // dS^T stored, one arrival per softmax warp
-  uint64_t* pt_free = bars + 15;     // dV MMAs done reading P^T (and every earlier MMA)
-  uint64_t* dst_free = bars + 16;    // dK MMAs done reading dS^T (and every earlier MMA)
-  uint64_t* drain = bars + 17;
-  uint64_t* info_full = bars + 18;   // [2], 32 arrivals (warp 3)
-  uint64_t* info_free = bars + 20;   // [2], one arrival per softmax warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+  uint64_t* pt_free = bars + 15;     // dV MMAs done reading P^T (and the earlier dV, dK ones)
+  uint64_t* dst_free = bars + 16;    // dK MMAs done reading dS^T (and the earlier dV, dK ones)
+  uint64_t* drain = bars + 17;       // [2], one per MMA issuer
+  uint64_t* info_full = bars + 19;   // [2], 32 arrivals (warp 3)
+  uint64_t* info_free = bars + 21;   // [2], one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* info_lse = reinterpret_cast<float*>(smem + INFO_OFF);  // [2][128]
   float* info_dl = info_lse + 2 * 128;                          // [2][128]
@@ -912,7 +922,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     for (int i = 0; i < DS; ++i) {
       mbar_init(&do_full[i], 1);
-      mbar_init(&do_empty[i], 1);
+      mbar_init(&do_empty[i], 2);  // released by a commit of each MMA issuer
     }
     mbar_init(sc_full, 1);
     mbar_init(sc_free, NSW);
@@ -920,7 +930,8 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(ds_full, NSW);
     mbar_init(pt_free, 1);
     mbar_init(dst_free, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&info_full[i], 32);
       mbar_init(&info_free[i], NSW);
@@ -993,31 +1004,36 @@ __global__ void __launch_bounds__(NT, 1)
           mbar_wait_bounded(&do_full[i], (uint32_t)armed_do[i], &none, err, SITE_ATTN,
                             timeout_ns / 8);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer
-    // Kept lean: this thread shares its scheduler with two softmax warps, and
-    // every instruction between two MMA groups is time the tensor pipe can
-    // run dry.  Descriptors are built once; a k-step or a ring stage only
-    // moves the 14-bit start-address field (shared memory < 256 KB: no carry).
+  } else if ((warp == 1 || warp == 2) && lane == 0) {
+    // ------------------------------------------------ MMA issuers
+    // Warp 1 issues the score products S^T(i) = K Q(i)^T and dP^T(i) =
+    // V dO(i)^T, warp 2 (idle between the TMEM allocation and release) the
+    // gradient products dV += P^T(i) dO(i) and dK += dS^T(i) Q(i).  An MMA
+    // issue holds its thread for about the MMA's run time, so one stream's
+    // waits and commits overlap the other stream's MMAs.  A commit tracks the
+    // MMAs of its own thread: dO(i) is read by dP^T(i) (warp 1) and dV(i)
+    // (warp 2, which only waits for P^T(i)), so its ring slot is released by
+    // a commit from each; Q(i) is last read by dK(i), which follows S^T(i)
+    // through the softmax warps' dS^T.  Descriptors are built once; a k-step
+    // or ring stage only moves the 14-bit start-address field (shared memory
+    // < 256 KB: no carry).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
     constexpr uint32_t idG = idesc_bf16_mn(false, true, BKV, HD);
     constexpr uint64_t kStage = 32768 >> 4;
-    const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
-    const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);    // K-major
-    const uint64_t dQm = sdesc_sw128(smem_u32(smem + Q_OFF), ATOM, 1024);  // MN-major
-    const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
-    const uint64_t dOm = sdesc_sw128(smem_u32(smem + DO_OFF), ATOM, 1024);
     // start-field offsets of k-step kk: K-major across 64-wide atoms, MN-major by 16 rows
     auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
     auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
     bool ok = sync.wait(kv_full, 0), issued = false;
-    int qs = 0, ds = 0, pqs = 0, pds = 0;  // ring stages of tiles i and i - 1
-    uint32_t qph = 0, dph = 0;
-    for (int i = 0; ok && i <= n_rt; ++i) {
-      const bool cur = i < n_rt, prev = i > 0;
-      if (cur) {  // S^T(i) once dP^T(i - 1) has been copied out of the score buffer
-        if (!sync.wait(&q_full[qs], qph) || (prev && !sync.wait(sc_free, 1))) {
+    if (warp == 1) {
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), 16, 1024);
+      const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);    // K-major
+      const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
+      for (int i = 0; ok && i < n_rt; ++i) {
+        const int qs = i % QS, ds = i % DS;
+        const uint32_t qph = (i / QS) & 1, dph = (i / DS) & 1;
+        // S^T(i) once dP^T(i - 1) has been copied out of the score buffer
+        if (!sync.wait(&q_full[qs], qph) || (i > 0 && !sync.wait(sc_free, 1))) {
           ok = false;
           break;
         }
@@ -1028,19 +1044,7 @@ __global__ void __launch_bounds__(NT, 1)
           umma_bf16(tmem, dK + koff(kk), bq + koff(kk), idS, kk > 0 ? 1u : 0u);
         umma_commit(sc_full);
         issued = true;
-      }
-      if (prev) {  // dV += P^T dO of tile i - 1
-        if (!sync.wait(p_full, (i - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t bo = dOm + pds * kStage;
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_bf16_tmem_a(tmem + 128, tmem + 384 + kk * 8, bo + moff(kk), idG,
-                           (i > 1 || kk > 0) ? 1u : 0u);
-        umma_commit(pt_free);
-        umma_commit(&do_empty[pds]);
-      }
-      if (cur) {  // dP^T(i) once S^T(i) has been copied out
+        // dP^T(i) once S^T(i) has been copied out
         if (!sync.wait(&do_full[ds], dph) || !sync.wait(sc_free, 0)) { ok = false; break; }
         tc_fence_after();
         const uint64_t bo = dOk + ds * kStage;
@@ -1048,27 +1052,41 @@ __global__ void __launch_bounds__(NT, 1)
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16(tmem, dV + koff(kk), bo + koff(kk), idS, kk > 0 ? 1u : 0u);
         umma_commit(sc_full);
+        umma_commit(&do_empty[ds]);
       }
-      if (prev) {  // dK += dS^T Q of tile i - 1
-        if (!sync.wait(ds_full, (i - 1) & 1)) { ok = false; break; }
+    } else {
+      const uint64_t dQm = sdesc_sw128(smem_u32(smem + Q_OFF), ATOM, 1024);  // MN-major
+      const uint64_t dOm = sdesc_sw128(smem_u32(smem + DO_OFF), ATOM, 1024);
+      for (int i = 0; ok && i < n_rt; ++i) {
+        const int qs = i % QS, ds = i % DS;
+        // dV += P^T dO of tile i, P^T read from tensor memory
+        if (!sync.wait(p_full, i & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t bq = dQm + pqs * kStage;
+        const uint64_t bo = dOm + ds * kStage;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          umma_bf16_tmem_a(tmem + 128, tmem + 384 + kk * 8, bo + moff(kk), idG,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(pt_free);
+        umma_commit(&do_empty[ds]);
+        issued = true;
+        // dK += dS^T Q of tile i
+        if (!sync.wait(ds_full, i & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bq = dQm + qs * kStage;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           umma_bf16_tmem_a(tmem + 256, tmem + 448 + kk * 8, bq + moff(kk), idG,
-                           (i > 1 || kk > 0) ? 1u : 0u);
+                           (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(dst_free);
-        umma_commit(&q_empty[pqs]);
+        umma_commit(&q_empty[qs]);
       }
-      pqs = qs;
-      pds = ds;
-      if (++qs == QS) { qs = 0; qph ^= 1u; }
-      if (++ds == DS) { ds = 0; dph ^= 1u; }
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      uint64_t* d = &drain[warp == 1 ? 0 : 1];
+      umma_commit(d);
+      mbar_wait_bounded(d, 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax warps

@@ -1012,9 +1012,10 @@ __global__ void __launch_bounds__(NT, 1)
     // issue holds its thread for about the MMA's run time, so one stream's
     // waits and commits overlap the other stream's MMAs.  A commit tracks the
     // MMAs of its own thread: dO(i) is read by dP^T(i) (warp 1) and dV(i)
-    // (warp 2, which only waits for P^T(i)), so its ring slot is released by
-    // a commit from each; Q(i) is last read by dK(i), which follows S^T(i)
-    // through the softmax warps' dS^T.  Descriptors are built once; a k-step
+    // (warp 2), so its ring slot is released by a commit from each; Q(i) is
+    // last read by dK(i), which follows S^T(i) through the softmax warps'
+    // dS^T.  Each issuer waits for every shared-memory operand it reads that
+    // its other waits do not already prove landed.  Descriptors are built once; a k-step
     // or ring stage only moves the 14-bit start-address field (shared memory
     // < 256 KB: no carry).
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BKV, BQ);
@@ -1059,8 +1060,13 @@ __global__ void __launch_bounds__(NT, 1)
       const uint64_t dOm = sdesc_sw128(smem_u32(smem + DO_OFF), ATOM, 1024);
       for (int i = 0; ok && i < n_rt; ++i) {
         const int qs = i % QS, ds = i % DS;
-        // dV += P^T dO of tile i, P^T read from tensor memory
-        if (!sync.wait(p_full, i & 1)) { ok = false; break; }
+        const uint32_t dph = (i / DS) & 1;
+        // dV += P^T dO of tile i, P^T read from tensor memory.  P^T(i) being
+        // stored says that S^T(i), hence Q(i), is done, but not that dO(i)
+        // has landed: wait for its slot here too.  (Its next fill needs this
+        // thread's release, so the parity cannot alias.)  dK(i) needs no such
+        // wait: dS^T(i) comes from dP^T(i), which read dO(i) after Q(i).
+        if (!sync.wait(p_full, i & 1) || !sync.wait(&do_full[ds], dph)) { ok = false; break; }
         tc_fence_after();
         const uint64_t bo = dOm + ds * kStage;
 #pragma unroll

@@ -203,9 +203,16 @@ __global__ void __launch_bounds__(kSegThreads)
   }
 }
 
-// One CTA per slice: if a segment cut by slice edges starts in this slice,
-// sum its partials slice by slice (fixed order) and write its dwte row.
-__global__ void __launch_bounds__(kSegThreads)
+// One CTA per (slice, group of columns): if a segment cut by slice edges
+// starts in this slice, sum its partials slice by slice (fixed order) and
+// write its dwte row.  The segment's last slice comes from a binary search
+// of the sorted ids, and the partials are loaded eight slices at a time
+// before they are added in order, so a long segment (the most frequent
+// token spans hundreds of slices) keeps several loads in flight.
+constexpr int kJoinThreads = 64;
+constexpr int kJoinBatch = 8;
+
+__global__ void __launch_bounds__(kJoinThreads)
     segment_join_kernel(const uint32_t* __restrict__ keys, const float* __restrict__ part_first,
                         const float* __restrict__ part_last, float* __restrict__ dwte, int M,
                         int d, int accumulate) {
@@ -215,27 +222,36 @@ __global__ void __launch_bounds__(kSegThreads)
   if (i0 + n >= M || keys[i0 + n] != v) return;  // the last run ends in this slice
   const bool whole_slice = keys[i0] == v;
   if (whole_slice && i0 > 0 && keys[i0 - 1] == v) return;  // began in an earlier slice
-  const int nslices = (M + kSlice - 1) / kSlice;
-  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-    float acc[4];
-    Vec4<float>::load((whole_slice ? part_first : part_last) + (long)s * d + c, acc);
-    for (int s2 = s + 1; s2 < nslices; ++s2) {
-      float t[4];
-      Vec4<float>::load(part_first + (long)s2 * d + c, t);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] += t[k];
-      const int e2 = min(M, (s2 + 1) * kSlice);
-      if (keys[e2 - 1] != v || e2 >= M || keys[e2] != v) break;  // the segment ends here
-    }
-    float* out = dwte + (long)v * d + c;
-    if (accumulate) {
-      float o[4];
-      Vec4<float>::load(out, o);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] += o[k];
-    }
-    Vec4<float>::store(out, acc);
+  const int c = (blockIdx.y * kJoinThreads + threadIdx.x) * 4;
+  if (c >= d) return;
+  // last index holding v: the keys are sorted
+  int lo = i0 + n, hi = M;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (keys[mid] <= v) lo = mid + 1; else hi = mid;
   }
+  const int s_end = (lo - 1) / kSlice;
+  float acc[4];
+  Vec4<float>::load((whole_slice ? part_first : part_last) + (long)s * d + c, acc);
+  for (int s2 = s + 1; s2 <= s_end; s2 += kJoinBatch) {
+    float t[kJoinBatch][4];
+#pragma unroll
+    for (int j = 0; j < kJoinBatch; ++j)
+      if (s2 + j <= s_end) Vec4<float>::load(part_first + (long)(s2 + j) * d + c, t[j]);
+#pragma unroll
+    for (int j = 0; j < kJoinBatch; ++j)
+      if (s2 + j <= s_end)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] += t[j][k];
+  }
+  float* out = dwte + (long)v * d + c;
+  if (accumulate) {
+    float o[4];
+    Vec4<float>::load(out, o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] += o[k];
+  }
+  Vec4<float>::store(out, acc);
 }
 
 // Rows of dwte whose id occurs in no token: zero (or left as they are when
@@ -320,8 +336,9 @@ cudaError_t embed_norm_bwd(bool bf16, const int* ids, const void* wte, const flo
   }
   segment_slice_kernel<<<nslices, kSegThreads, 0, ctx.stream>>>(k0, v0, dx0, dwte, part_first,
                                                                 part_last, M, d, accumulate);
-  segment_join_kernel<<<nslices, kSegThreads, 0, ctx.stream>>>(k0, part_first, part_last, dwte, M,
-                                                               d, accumulate);
+  const dim3 jgrid(nslices, (unsigned)((d + 4 * kJoinThreads - 1) / (4 * kJoinThreads)));
+  segment_join_kernel<<<jgrid, kJoinThreads, 0, ctx.stream>>>(k0, part_first, part_last, dwte, M,
+                                                              d, accumulate);
   return launched(2);
 }
 

@@ -5,6 +5,8 @@
         --M 16384 --N 5120 --K 1280 --iters 3
     python -m pretraining_step_pretrain_b300.profile_cases attn --B 4 --T 2048 --H 10 --bwd
     python -m pretraining_step_pretrain_b300.profile_cases step --workload small_bf16
+    python -m pretraining_step_pretrain_b300.profile_cases step --workload d20_bf16 --depth 1 \
+        --vocab 4096 --iters 2
     python -m pretraining_step_pretrain_b300.profile_cases gemm_fp8 --M 65536 --N 5120 --K 1280
 
 The gemm and gemm_fp8 cases also print the mean time and FLOP rate of their
@@ -107,18 +109,29 @@ def attn(a):
 
 
 def step(a):
+    """nc_step on a named workload; --depth / --vocab / --batch / --seq override its
+    shape (e.g. one block at the depth-20 widths, for captures of every kernel
+    of a step on inputs larger than L2 but a few GB on the device)."""
+    import dataclasses
+
     import nc_synth
     w = nc_synth.WORKLOADS[a.workload]
-    ids, tg = nc_synth.make_tokens(w.shape.vocab, w.batch, w.seq, seed=0, dist=w.ids)
-    st = nc.Step(w.shape, w.dtype, w.batch, w.seq,
-                 nc_synth.make_weights(w.shape, seed=1, bf16=(w.dtype == "bf16")))
+    shape = w.shape
+    if a.depth:
+        shape = dataclasses.replace(shape, depth=a.depth)
+    if a.vocab:
+        shape = dataclasses.replace(shape, vocab=a.vocab)
+    B, T = a.batch or w.batch, a.seq or w.seq
+    ids, tg = nc_synth.make_tokens(shape.vocab, B, T, seed=0, dist=w.ids)
+    st = nc.Step(shape, w.dtype, B, T, nc_synth.make_weights(shape, seed=1, bf16=(w.dtype == "bf16")))
     st.ids.copy_(torch.from_numpy(ids))
     st.targets.copy_(torch.from_numpy(tg))
     for _ in range(a.iters):
         st.run()
     torch.cuda.synchronize()
     assert st.status() == 0
-    print(f"step {a.workload}: loss {float(st.loss.item()):.5f}")
+    print(f"step {a.workload} depth={shape.depth} V={shape.vocab} B={B} T={T}: "
+          f"loss {float(st.loss.item()):.5f}, {nc.launch_count() // max(a.iters, 1)} launches per step")
 
 
 def main():
@@ -145,6 +158,10 @@ def main():
     p = sub.add_parser("step")
     p.add_argument("--workload", default="small_bf16")
     p.add_argument("--iters", type=int, default=2)
+    p.add_argument("--depth", type=int, default=0)
+    p.add_argument("--vocab", type=int, default=0)
+    p.add_argument("--batch", type=int, default=0)
+    p.add_argument("--seq", type=int, default=0)
     a = ap.parse_args()
     {"gemm": gemm, "gemm_fp8": gemm_fp8, "attn": attn, "step": step}[a.case](a)
 

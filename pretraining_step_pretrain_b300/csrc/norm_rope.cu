@@ -174,11 +174,9 @@ __global__ void qknorm_rope_fwd_kernel(const A* __restrict__ qkv, const float2* 
                                        float* __restrict__ rstd_qk, int M, int T, int H,
                                        float eps) {
   // One warp per token: H query heads, the key head, the value head.  The
-  // token's (cos, sin) pairs are read once; eight heads (the whole token at
-  // the depth-20 shape) are loaded before any is used so that many loads are
-  // in flight per lane.
+  // token's (cos, sin) pairs are read once; four heads are loaded before any
+  // is used so that several loads are in flight per lane.
   constexpr int h = 32 * E, half = h / 2;
-  constexpr int kHeadsInFlight = 8;
   const int m = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (m >= M) return;
@@ -189,13 +187,13 @@ __global__ void qknorm_rope_fwd_kernel(const A* __restrict__ qkv, const float2* 
   for (int e = 0; e < E; ++e) cs[e] = tab[(long)t * half + (lane & 15) * E + e];
   const int nh = H + 2;
   const A* src = qkv + (long)m * nh * h + lane * E;
-  for (int j0 = 0; j0 < nh; j0 += kHeadsInFlight) {
-    float x[kHeadsInFlight][E];
+  for (int j0 = 0; j0 < nh; j0 += 4) {
+    float x[4][E];
 #pragma unroll
-    for (int u = 0; u < kHeadsInFlight; ++u)
+    for (int u = 0; u < 4; ++u)
       if (j0 + u < nh) load_vec<A, E>(src + (long)(j0 + u) * h, x[u]);
 #pragma unroll
-    for (int u = 0; u < kHeadsInFlight; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int j = j0 + u;
       if (j >= nh) break;
       if (j == H + 1) {

@@ -13,6 +13,8 @@
 //   Out         element type of the destination.
 #pragma once
 
+#include <cuda.h>
+
 #include "nc_common.cuh"
 
 namespace nc {
@@ -279,6 +281,78 @@ struct EpiSoftcapCE {
   }
   __device__ __forceinline__ void row_end(int row, int col0, float sum) const {
     part[(long)row * n_part + col0 / tile_n] = sum;
+  }
+};
+
+// QK-norm + RoPE fused into the QKV projection (launch article, architecture
+// list: QK norm -- RMSNorm of every query head and of the key head -- and
+// rotary embeddings).  The tensor-core kernel hands this epilogue one head at
+// a time: the 128 fp32 accumulators of a row's head, as two 64-column chunks.
+// Query heads (head < H) and the key head (head == H) are RMS-normalised over
+// their 128 values and rotated by the token's position t = row % T: the
+// half-split pairs (i, i + 64) are element i of the first chunk and element i
+// of the second, rotated by angle t theta_i with (cos, sin) from the step's
+// table; rstd_qk[row][head] keeps the normaliser for the backward.  The value
+// head passes through.  Each chunk goes by its own tensor map to q (M, H h),
+// k (M, h) or v (M, h), the layouts the attention kernels read.
+struct EpiQkNormRope {
+  static constexpr bool kRowReduce = false;
+  static constexpr bool kHeadPairs = true;
+  using Out = bf16;
+  CUtensorMap mq, mk, mv;
+  // (T, 64) pairs (cos, sin) of t theta_i as fp16 (an fp16 value carries a
+  // 2^-11 relative error, a quarter of the bf16 rounding of the stored q and
+  // k).  The kernel copies the 128 rows of a half tile into shared memory by
+  // TMA (two 128-byte-swizzled [128 rows][128 B] chunks: pairs 0-31 and
+  // 32-63), so T must be a multiple of 128.
+  const __half2* tab;
+  float* rstd_qk;     // (M, H + 1)
+  int T, H;
+  float eps;
+  __device__ __forceinline__ bool reduce() const { return false; }
+  __device__ __forceinline__ void row_end(int, int, float) const {}
+  // Head `head` of output row `row`: a = its columns 0-63, b = 64-127; `tab`
+  // holds the table rows of the half tile, this row's at index r.
+  __device__ __forceinline__ void compute_head(int row, int head, float (&a)[64],
+                                               float (&b)[64], const uint8_t* tab,
+                                               int r) const {
+    if (head > H) return;  // the value head: stored as computed
+    float s8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) s8[i & 7] = fmaf(a[i], a[i], fmaf(b[i], b[i], s8[i & 7]));
+    const float ss = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    const float rs = rsqrtf(ss / 128.f + eps);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint8_t* trow = tab + j * (128 * 128) + r * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(trow + ((q ^ (r & 7)) << 4));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+          const int k = 32 * j + 4 * q + e;
+          const float y0 = a[k] * rs, y1 = b[k] * rs;
+          a[k] = y0 * c2.x - y1 * c2.y;
+          b[k] = y0 * c2.y + y1 * c2.x;
+        }
+      }
+    }
+    rstd_qk[(long)row * (H + 1) + head] = rs;
+  }
+  // Destination of the 64-column chunk starting at column `col` of the
+  // (M, (H + 2) 128) product, and the chunk's first column there.
+  __device__ __forceinline__ const CUtensorMap* dest(int col, int& x) const {
+    const int head = col >> 7;
+    if (head < H) {
+      x = col;
+      return &mq;
+    }
+    x = col & 127;
+    return head == H ? &mk : &mv;
   }
 };
 

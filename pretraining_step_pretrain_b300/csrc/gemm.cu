@@ -247,13 +247,16 @@ cudaError_t launch_tc(const GemmArgs& g, const Plan& p, const Epi& epi, void* ou
   // Auxiliary operand (same layout as C) for the epilogues that read one;
   // the others get C's map, unused.
   constexpr bool kAux = tc::HasAuxTma<Epi>::value;
+  constexpr bool kHeads = tc::HasHeadPairs<Epi>::value;
   CUtensorMap tax = tcm;
-  if (kAux)
+  if constexpr (kAux)
     ok = ok && make_tmap_out<typename Epi::Out>(&tax, const_cast<void*>(g.aux), g.N, g.M, ldo,
                                                 nb, nb > 1 ? g.c_bstride : 0);
+  if constexpr (kHeads)  // the (T, 128) fp16 table, [128 rows][64 values] boxes
+    ok = ok && make_tmap_out<__half>(&tax, const_cast<__half2*>(epi.tab), 128, epi.T, 128, 1);
   if (!ok) return cudaErrorInvalidValue;
   auto kern = tc::gemm_bf16_tc_kernel<A_MN, B_MN, Epi>;
-  constexpr int smem_bytes = tc::SmemPlan<kAux>::BYTES;
+  constexpr int smem_bytes = tc::SmemPlan<kAux || kHeads>::BYTES;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e =
@@ -396,6 +399,25 @@ cudaError_t gemm_bf16(const GemmArgs& g, const Ctx& ctx) {
       EpiAxpby<bf16> e{static_cast<bf16*>(g.C), aux, g.ldc, g.batch > 1 ? g.c_bstride : 0,
                        g.alpha, g.beta};
       return dispatch_tc(g, p, e, g.C, g.ldc, 1, ctx);
+    }
+    case EPI_QKNORM_ROPE: {
+      // NT only; C (the (M, (H + 2) 128) product) is only the kernel's unused
+      // default map: the heads go to q, k, v through the epilogue's maps.
+      const long Hh = (long)g.qk_H * 128;
+      if (g.layout != GEMM_NT || g.N != (g.qk_H + 2) * 128 || g.batch > 1 || !g.qk_q ||
+          !g.qk_k || !g.qk_v || !g.qk_rstd || !g.qk_tab || g.qk_T < 1 || g.qk_T % 128 != 0)
+        return cudaErrorInvalidValue;
+      EpiQkNormRope e;
+      if (!make_tmap_out<bf16>(&e.mq, g.qk_q, Hh, g.M, Hh, 1) ||
+          !make_tmap_out<bf16>(&e.mk, g.qk_k, 128, g.M, 128, 1) ||
+          !make_tmap_out<bf16>(&e.mv, g.qk_v, 128, g.M, 128, 1))
+        return cudaErrorInvalidValue;
+      e.tab = static_cast<const __half2*>(g.qk_tab);
+      e.rstd_qk = g.qk_rstd;
+      e.T = g.qk_T;
+      e.H = g.qk_H;
+      e.eps = g.qk_eps;
+      return launch_tc<false, false>(g, p, e, g.C, g.ldc, 1, ctx);
     }
   }
   return cudaErrorInvalidValue;

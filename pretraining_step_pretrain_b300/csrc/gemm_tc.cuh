@@ -52,6 +52,7 @@ constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 // Epilogue staging: two 128-row x 128-byte chunks of the output tile, and
 // for epilogues with an auxiliary operand (same layout as C) two more for
 // its chunks, loaded by TMA ahead of use; those run a 5-stage operand ring.
+// Head-pair epilogues use the same two extra chunks for their per-row table.
 constexpr int STAGE_OUT_BYTES = HALF_ROWS * 128;  // 16 KB
 template <bool kAux>
 struct SmemPlan {
@@ -132,6 +133,16 @@ template <class E>
 struct HasAuxTma<E, std::void_t<decltype(E::kAuxTma)>> {
   static constexpr bool value = E::kAuxTma;
 };
+// Epilogues that declare kHeadPairs take two 64-column chunks of a row at a
+// time (compute_head) and choose each chunk's destination map (dest).
+template <class E, class = void>
+struct HasHeadPairs {
+  static constexpr bool value = false;
+};
+template <class E>
+struct HasHeadPairs<E, std::void_t<decltype(E::kHeadPairs)>> {
+  static constexpr bool value = E::kHeadPairs;
+};
 
 enum WaitSite : int {
   SITE_PROD_EMPTY = 101, SITE_MMA_ACC_EMPTY = 102, SITE_MMA_FULL = 103,
@@ -189,10 +200,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmAux, const Sched sch, const int M,
-                        const int N, const Epi epi, int* err, const long long timeout_ns) {
+                        const int N, const __grid_constant__ Epi epi, int* err,
+                        const long long timeout_ns) {
   static_assert(!kFp8 || (!A_MN && !B_MN), "8-bit operands are K-major");
   constexpr bool kAux = HasAuxTma<Epi>::value;
-  using Plan = SmemPlan<kAux>;
+  constexpr bool kHeads = HasHeadPairs<Epi>::value;
+  using Plan = SmemPlan<kAux || kHeads>;
   constexpr int STAGES = Plan::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -234,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (kAux) tma_prefetch_desc(&tmAux);
+    if (kAux || kHeads) tma_prefetch_desc(&tmAux);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -374,6 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t aux_uses[2] = {0, 0};    // loads consumed per auxiliary buffer
     uint32_t aux_issued[2] = {0, 0};  // loads issued per auxiliary buffer (issuer)
     uint32_t acc_phase = 0;
+    uint32_t tab_loads = 0;           // head pairs: table loads waited for so far
     for (int u = pair; u < sch.units; u += npairs) {
       int mt, nt, split, batch, kb0, kb1;
       sch.decode(u, mt, nt, split, batch, kb0, kb1);
@@ -395,6 +409,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (issuer)
           for (int c = 0; c < min(2, nvalid); ++c) issue_aux(c);
       }
+      if constexpr (kHeads) {
+        // The half tile's 128 table rows, while the tile still accumulates.
+        // Every thread finished reading the previous unit's rows before the
+        // named barrier that preceded its first staged chunk; tiles without
+        // a head (nvalid == 0) neither load nor wait.
+        if (issuer && nvalid > 0) {
+          ++aux_issued[0];
+          mbar_arrive_expect_tx(&aux_full[0], 2 * STAGE_OUT_BYTES);
+          const int t0 = row0 % epi.T;
+          tma_load_3d(smem + Plan::AUX_OFF, &tmAux, &aux_full[0], 0, t0, 0);
+          tma_load_3d(smem + Plan::AUX_OFF + STAGE_OUT_BYTES, &tmAux, &aux_full[0], 64, t0, 0);
+        }
+      }
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait_cluster(&acc_full[acc], acc_phase, abort_flag, err, SITE_EPI_ACC_FULL,
@@ -409,6 +436,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       float row_acc = 0.f;
+      if constexpr (HasHeadPairs<Epi>::value) {
+        // One head (two 64-column chunks) at a time; each chunk is staged and
+        // stored like any other, to the destination the epilogue names.
+        static_assert(W == 64 && !kAux, "head pairs are 64-column bf16 chunks");
+        int tok = 1;
+        if (nvalid > 0) {
+          if (lane == 0)
+            tok = mbar_wait_bounded(&aux_full[0], tab_loads & 1u, abort_flag, err,
+                                    SITE_EPI_ACC_FULL, timeout_ns);
+          tok = __shfl_sync(0xffffffffu, tok, 0);
+          if (tok) mbar_try_wait(smem_u32(&aux_full[0]), tab_loads & 1u);  // acquire in every lane
+          ++tab_loads;
+        }
+#pragma unroll 1
+        for (int c = 0; c + 1 < nvalid; c += 2) {
+          const int col = nt * BN + c * W;
+          float v0[64], v1[64];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_32cols(taddr + c * W + h * 32, *reinterpret_cast<float(*)[32]>(v0 + h * 32));
+            tmem_ld_32cols(taddr + (c + 1) * W + h * 32,
+                           *reinterpret_cast<float(*)[32]>(v1 + h * 32));
+          }
+          if (row < M && tok)
+            epi.compute_head(row, col >> 7, v0, v1, smem + Plan::AUX_OFF, r_in);
+#pragma unroll 1
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint8_t* chunk = smem + Plan::OUT_OFF + (chunk_no & 1) * STAGE_OUT_BYTES;
+            ++chunk_no;
+            if (issuer) bulk_wait_group_read<1>();  // the store issued from this buffer is done reading
+            named_bar_sync<128>();
+            if (q2 == 0)
+              stage_row<Out, W>(chunk, r_in, v0);
+            else
+              stage_row<Out, W>(chunk, r_in, v1);
+            fence_proxy_async_smem();
+            named_bar_sync<128>();
+            if (issuer) {
+              int x = 0;
+              const CUtensorMap* dmap = epi.dest(col + q2 * W, x);
+              tma_store_3d(dmap, chunk, x, row0, 0);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int c = 0; c < nvalid; ++c) {
         const int col = nt * BN + c * W;
@@ -454,6 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      }
       if (Epi::kRowReduce && row < M) epi.row_end(row, nt * BN, row_acc);
       tc_fence_before();
       __syncwarp();
@@ -466,6 +540,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (issuer) {
       bulk_wait_group_all();
       // After an abort: let auxiliary loads already issued land before exit.
+      if constexpr (kHeads) {
+        int none = 0;
+        for (; tab_loads < aux_issued[0]; ++tab_loads)
+          mbar_wait_bounded(&aux_full[0], tab_loads & 1u, &none, err, SITE_DRAIN,
+                            timeout_ns / 8);
+      }
       if constexpr (kAux) {
         int none = 0;
         for (int b2 = 0; b2 < 2; ++b2)

@@ -114,7 +114,7 @@ struct LayerBufs {
 
 struct Layout {
   size_t total = 0;
-  size_t err, rope, rstd0, x, dx, xf, rstdf, big, part, lse_row, s_tgt, loss_misc;
+  size_t err, rope, rope16, rstd0, x, dx, xf, rstdf, big, part, lse_row, s_tgt, loss_misc;
   size_t qkv, dx_act, dxn, du, dact, delta, split;
   size_t layer0, layer_stride;
   size_t l_xn, l_q, l_k, l_v, l_o, l_xn2, l_a, l_rstd1, l_rstd_qk, l_lse, l_rstd2;
@@ -135,6 +135,7 @@ Layout make_layout(const nc_config& c, int B, int T) {
   auto take = [&](size_t bytes) { size_t r = o; o += al(bytes); return r; };
   L.err = take(256);
   L.rope = take(T * (h / 2) * 8);
+  L.rope16 = take(T * (h / 2) * 4);
   L.rstd0 = take(M * 4);
   L.x = take(M * d * 4);
   L.dx = take(M * d * 4);
@@ -247,7 +248,7 @@ nc_status embed_fwd_impl(const nc_config& c, int B, int T, const int32_t* ids, c
                          float* x, void* ws, const Layout& L, const Ctx& ctx) {
   const bool bf = c.dtype == NC_BF16;
   NC_CUDA(cudaMemsetAsync(ws, 0, 16, ctx.stream));
-  NC_RUN("embed.rope_table", rope_table(at<float2>(ws, L.rope), T, c.head_dim, c.rope_base, ctx));
+  NC_RUN("embed.rope_table", rope_table(at<float2>(ws, L.rope), at(ws, L.rope16), T, c.head_dim, c.rope_base, ctx));
   NC_RUN("embed.norm", embed_norm_fwd(bf, ids, wte, x, at<float>(ws, L.rstd0), L.M, c.d_model, c.vocab, c.eps,
                          ctx));
   return NC_OK;
@@ -261,10 +262,25 @@ nc_status block_fwd_impl(const nc_config& c, int layer, int B, int T, const nc_l
   LayerBufs lb = layer_bufs(ws, L, layer);
   void* qkv = at(ws, L.qkv);
   NC_RUN("fwd.norm1", rmsnorm_fwd(bf, x, lb.xn, lb.rstd1, M, d, c.eps, ctx));
-  NC_RUN("fwd.qkv_gemm", run_gemm(bf, gemm_args(GEMM_NT, EPI_STORE, M, qkvw, d, lb.xn, d, w.w_qkv, d, qkv, qkvw),
-                   &L, ws, ctx));
-  NC_RUN("fwd.qknorm_rope", qknorm_rope_fwd(bf, qkv, at<float2>(ws, L.rope), lb.q, lb.k, lb.v, lb.rstd_qk, B, T, H,
-                          h, c.eps, ctx));
+  if (bf && h == 128 && T % 128 == 0) {
+    // QK-norm + RoPE in the QKV GEMM's epilogue, straight into q, k, v (each
+    // 128-row half tile reads 128 consecutive positions of the RoPE table).
+    GemmArgs g = gemm_args(GEMM_NT, EPI_QKNORM_ROPE, M, qkvw, d, lb.xn, d, w.w_qkv, d, qkv, qkvw);
+    g.qk_q = lb.q;
+    g.qk_k = lb.k;
+    g.qk_v = lb.v;
+    g.qk_rstd = lb.rstd_qk;
+    g.qk_tab = at(ws, L.rope16);
+    g.qk_T = T;
+    g.qk_H = H;
+    g.qk_eps = c.eps;
+    NC_RUN("fwd.qkv_gemm", run_gemm(bf, g, &L, ws, ctx));
+  } else {
+    NC_RUN("fwd.qkv_gemm", run_gemm(bf, gemm_args(GEMM_NT, EPI_STORE, M, qkvw, d, lb.xn, d, w.w_qkv, d, qkv, qkvw),
+                     &L, ws, ctx));
+    NC_RUN("fwd.qknorm_rope", qknorm_rope_fwd(bf, qkv, at<float2>(ws, L.rope), lb.q, lb.k, lb.v, lb.rstd_qk, B, T, H,
+                            h, c.eps, ctx));
+  }
   NC_RUN("fwd.attention", attention_fwd(bf, B, T, H, h, lb.q, lb.k, lb.v, lb.o, lb.lse, ctx));
   NC_RUN("fwd.out_gemm", run_gemm(bf, gemm_args(GEMM_NT, EPI_ADD_F32, M, d, H * h, lb.o, H * h, w.w_o, H * h, x, d),
                    &L, ws, ctx));

@@ -31,7 +31,7 @@ constexpr long kMaxAttnRowsPerSeq = 65534L * 128;
 
 enum GemmLayout { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
 enum GemmEpi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_ADD_F32 = 2, EPI_RELU2 = 3,
-               EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5, EPI_AXPBY = 6 };
+               EPI_RELU2_BWD = 4, EPI_SOFTCAP_CE = 5, EPI_AXPBY = 6, EPI_QKNORM_ROPE = 7 };
 
 struct GemmArgs {
   int layout, epi;
@@ -52,6 +52,13 @@ struct GemmArgs {
   int batch;
   long a_bstride, b_bstride, c_bstride;
   float alpha, beta;      // AXPBY: C = alpha * aux + beta * acc
+  // QKNORM_ROPE (tensor-core path, head_dim 128): the QKV product's heads go
+  // normalised and rotated to q (M, H 128), k, v (M, 128); rstd_qk (M, H + 1)
+  void *qk_q, *qk_k, *qk_v;
+  float* qk_rstd;
+  const void* qk_tab;     // fp16 pairs (T, 64): cos, sin
+  int qk_T, qk_H;
+  float qk_eps;
 };
 
 // bf16 tensor map with 128-byte swizzle and zero fill out of range.  dims[0]
@@ -70,7 +77,9 @@ cudaError_t gemm_f32(const GemmArgs& g, const Ctx& ctx);
 
 // ---- memory-bound kernels (act = bf16 or float) ----
 // Each takes `bf16` to pick the activation type.
-cudaError_t rope_table(float2* tab, int T, int h, float base, const Ctx& ctx);
+// cos, sin of t theta_i for t < T, i < h/2: float2 (T, h/2) in `tab`, and the
+// same as fp16 pairs in `tab16` (may be null) for the QKV epilogue.
+cudaError_t rope_table(float2* tab, void* tab16, int T, int h, float base, const Ctx& ctx);
 cudaError_t embed_norm_fwd(bool bf16, const int* ids, const void* wte, float* x, float* rstd,
                            int M, int d, int V, float eps, const Ctx& ctx);
 cudaError_t rmsnorm_fwd(bool bf16, const float* x, void* y, float* rstd, int M, int d, float eps,

@@ -42,7 +42,8 @@ __device__ __forceinline__ void store_vec(A* p, const float (&x)[E]) {
 }
 
 // ---- RoPE table: tab[t * h/2 + i] = (cos, sin)(t * base^(-2i/h)), fp64 math.
-__global__ void rope_table_kernel(float2* tab, int T, int half, int h, double base) {
+__global__ void rope_table_kernel(float2* tab, __half2* tab16, int T, int half, int h,
+                                  double base) {
   const long n = (long)T * half;
   for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < n;
        idx += (long)gridDim.x * blockDim.x) {
@@ -51,6 +52,7 @@ __global__ void rope_table_kernel(float2* tab, int T, int half, int h, double ba
     double s, c;
     sincos((double)t * theta, &s, &c);
     tab[idx] = make_float2((float)c, (float)s);
+    if (tab16) tab16[idx] = __floats2half2_rn((float)c, (float)s);
   }
 }
 
@@ -422,10 +424,11 @@ inline int staged_blocks(long M, int smem, int num_sms) {
 
 }  // namespace
 
-cudaError_t rope_table(float2* tab, int T, int h, float base, const Ctx& ctx) {
+cudaError_t rope_table(float2* tab, void* tab16, int T, int h, float base, const Ctx& ctx) {
   const long n = (long)T * (h / 2);
   const int blocks = (int)std::min<long>((n + 255) / 256, 4096);
-  rope_table_kernel<<<blocks, 256, 0, ctx.stream>>>(tab, T, h / 2, h, (double)base);
+  rope_table_kernel<<<blocks, 256, 0, ctx.stream>>>(tab, static_cast<__half2*>(tab16), T, h / 2,
+                                                    h, (double)base);
   return launched(1);
 }
 

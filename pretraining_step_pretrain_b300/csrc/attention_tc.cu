@@ -119,77 +119,113 @@ struct CtaSync {
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) const {
     return mbar_wait_bounded(bar, parity, abort_flag, err, SITE_ATTN, timeout_ns);
   }
+  // The same wait with one outcome for the whole warp (called by all 32
+  // lanes): a warp that goes on to a warp-collective tcgen05.ld/st must not
+  // split when some lanes give up at the limit and others do not.
+  __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) const {
+    return __all_sync(0xffffffffu, wait(bar, parity));
+  }
 };
 
 // ======================================================================
-// forward: 128 packed query rows per CTA, 128-key tiles
+// forward: persistent CTAs, one per SM, each walking a list of query-tile
+// pairs (tile 0: packed rows r0 .. r0 + 127, tile 1: the next 128) of every
+// sequence, heaviest pairs first and the order reversed every other round so
+// that the CTAs get similar shares of key tiles; per pair one stream of
+// 128-key tiles serves both query tiles.  The rings and barrier phases carry
+// on from one pair to the next, so the next pair's loads and first score
+// products overlap the current pair's output epilogue.
 // ======================================================================
 namespace fwd {
 constexpr int BQ = 128, BKV = 128;
-constexpr int NG = 4;                       // softmax column groups (4 warps each)
-constexpr int CW = BKV / NG;                // key columns per softmax thread
-constexpr int NSWF = 4 * NG;                // softmax warps (warps 4 .. 4 + NSWF - 1)
-constexpr int NTF = 32 * (4 + NSWF);        // threads per CTA
+constexpr int NTF = 352;                    // 3 control warps + one softmax warpgroup per tile
 constexpr int ATOM = 16384;                 // [128 rows][64] bf16
-constexpr int Q_OFF = 0;                    // 32 KB
-constexpr int K_OFF = 32768;                // 2 x 32 KB
-constexpr int V_OFF = K_OFF + 2 * 32768;    // 2 x 32 KB
-constexpr int RED_OFF = V_OFF + 2 * 32768;  // [2 parity][NG][128] row maxima
-constexpr int LSUM_OFF = RED_OFF + 2 * NG * 128 * 4;  // [NG][128] row sums
-constexpr int BAR_OFF = LSUM_OFF + NG * 128 * 4;
+constexpr int Q_OFF = 0;                    // 2 tiles x 32 KB
+constexpr int K_OFF = 2 * 32768;            // 2 stages x 32 KB
+constexpr int V_OFF = K_OFF + 2 * 32768;    // 2 stages x 32 KB
+constexpr int BAR_OFF = V_OFF + 2 * 32768;
 constexpr int SMEM = BAR_OFF + 256 + 1024;
+static_assert(SMEM <= 232448, "forward shared memory exceeds 227 KB");
 }  // namespace fwd
 
+// fma on both halves of a packed fp32 pair.
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, r;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 r, a, b, c;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Work item k of CTA c among G persistent CTAs: round k takes items k G ..
+// k G + G - 1, forwards in even rounds and backwards in odd ones.
+__device__ __forceinline__ long snake_item(int c, int k, int G, long n_items) {
+  const long u = (long)k * G + ((k & 1) ? G - 1 - c : c);
+  return u < n_items ? u : -1;
+}
+
+// Tensor memory (512 columns): S of tile x at columns 128 x, O of tile x at
+// 256 + 128 x.  P(j) of a tile, bf16 pairs, overwrites the first 64 columns
+// of its S once the softmax threads have read S(j); so the tile's next score
+// product is issued only after the P V product that reads P(j) has
+// completed.  While one tile's softmax runs, the tensor pipe works on the
+// other tile's products.
 __global__ void __launch_bounds__(fwd::NTF, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ o,
-                       float* __restrict__ lse, int T, int H, int* err, long long timeout_ns) {
+                       float* __restrict__ lse, int B, int T, int H, int* err,
+                       long long timeout_ns) {
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2], one arrival per softmax warp
-  uint64_t* p_full = bars + 13;   // [2] by P buffer, one arrival per softmax warp
-  uint64_t* pv_done = bars + 15;  // [2] by P buffer: the PV MMA that read it is done
-  uint64_t* drain = bars + 17;     // [2], one per MMA issuer
-  uint64_t* red_full = bars + 19;  // [2], one arrival per softmax warp
-  uint64_t* lsum_full = bars + 21; // one arrival per softmax warp
+  uint64_t* q_full = bars + 0;    // [2] by tile
+  uint64_t* q_empty = bars + 2;   // [2] by tile: the pair's last score product is done
+  uint64_t* k_full = bars + 4;    // [2] by stage
+  uint64_t* k_empty = bars + 6;   // [2] by stage, one commit per tile
+  uint64_t* v_full = bars + 8;    // [2]
+  uint64_t* v_empty = bars + 10;  // [2]
+  uint64_t* s_full = bars + 12;   // [2] by tile
+  uint64_t* p_full = bars + 14;   // [2] by tile, one arrival per softmax warp
+  uint64_t* pv_done = bars + 16;  // [2] by tile
+  uint64_t* drain = bars + 18;    // [2] by tile (its MMA issuer)
+  uint64_t* s0_read = bars + 20;  // [2] by tile 0's step parity: its softmax has read S
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x;  // batch fastest: every row's heaviest tiles launch first
   const long TH = (long)T * H;
-  const int n_qt = (int)((TH + BQ - 1) / BQ);
-  const long r0 = (long)(n_qt - 1 - blockIdx.y) * BQ;  // heaviest tiles first
-  const int t_last = (int)(min(r0 + BQ - 1, TH - 1) / H);
-  const int nkv = t_last / BKV + 1;
+  const int n_pairs = (int)((TH + 2 * BQ - 1) / (2 * BQ));
+  const long n_items = (long)B * n_pairs;
+  const int G = gridDim.x, cta = blockIdx.x;
+  // Item u: sequence u % B (fastest, so concurrent CTAs share no K/V), pair
+  // n_pairs - 1 - u / B (the heaviest first).
+  auto item_b = [&](long u) { return (int)(u % B); };
+  auto item_r0 = [&](long u) { return (long)(n_pairs - 1 - (int)(u / B)) * 2 * BQ; };
+  // Key tiles query tile x of an item sees (up to its last row's token); the
+  // K/V stream runs to tile 1's count, at most one more than tile 0's.
+  auto key_tiles = [&](long u, int x) {
+    const long last = min(item_r0(u) + (long)(x + 1) * BQ - 1, TH - 1);
+    return (int)(last / H) / BKV + 1;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], 2);
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+      mbar_init(&v_empty[i], 2);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSWF);
-      mbar_init(&p_full[i], NSWF);
+      mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&drain[i], 1);
+      mbar_init(&s0_read[i], 4);
     }
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
-    mbar_init(&red_full[0], NSWF);
-    mbar_init(&red_full[1], NSWF);
-    mbar_init(lsum_full, NSWF);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -205,199 +241,243 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
-    int armed[5] = {-1, -1, -1, -1, -1};  // q, k0, k1, v0, v1 parities for the drain
-    mbar_arrive_expect_tx(q_full, 2 * ATOM);
-    tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, (int)r0, b);
-    tma_load_3d(smem + Q_OFF + ATOM, &tmQ, q_full, 64, (int)r0, b);
-    armed[0] = 0;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&k_empty[st], ph ^ 1u)) break;
-      mbar_arrive_expect_tx(&k_full[st], 2 * ATOM);
-      tma_load_3d(smem + K_OFF + st * 32768, &tmK, &k_full[st], 0, j * BKV, b);
-      tma_load_3d(smem + K_OFF + st * 32768 + ATOM, &tmK, &k_full[st], 64, j * BKV, b);
-      armed[1 + st] = (int)ph;
-      if (!sync.wait(&v_empty[st], ph ^ 1u)) break;
-      mbar_arrive_expect_tx(&v_full[st], 2 * ATOM);
-      tma_load_3d(smem + V_OFF + st * 32768, &tmV, &v_full[st], 0, j * BKV, b);
-      tma_load_3d(smem + V_OFF + st * 32768 + ATOM, &tmV, &v_full[st], 64, j * BKV, b);
-      armed[3 + st] = (int)ph;
+    int armed[6] = {-1, -1, -1, -1, -1, -1};  // q0, q1, k0, k1, v0, v1 parities for the drain
+    long g = 0;  // key tiles streamed so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const long u = snake_item(cta, k, G, n_items);
+      if (u < 0) break;
+      const int b = item_b(u);
+      const long r0 = item_r0(u);
+      const int nkv = key_tiles(u, 1);
+      for (int x = 0; x < 2 && ok; ++x) {
+        // The previous pair's last score product of this tile has read Q.
+        if (k > 0 && !sync.wait(&q_empty[x], (k - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&q_full[x], 2 * ATOM);
+        const int y = (int)(r0 + x * BQ);  // rows past the sequence read as zero
+        tma_load_3d(smem + Q_OFF + x * 32768, &tmQ, &q_full[x], 0, y, b);
+        tma_load_3d(smem + Q_OFF + x * 32768 + ATOM, &tmQ, &q_full[x], 64, y, b);
+        armed[x] = k & 1;
+      }
+      for (int j = 0; ok && j < nkv; ++j, ++g) {
+        const int st = (int)(g & 1);
+        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        if (!sync.wait(&k_empty[st], ph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[st], 2 * ATOM);
+        tma_load_3d(smem + K_OFF + st * 32768, &tmK, &k_full[st], 0, j * BKV, b);
+        tma_load_3d(smem + K_OFF + st * 32768 + ATOM, &tmK, &k_full[st], 64, j * BKV, b);
+        armed[2 + st] = (int)ph;
+        if (!sync.wait(&v_empty[st], ph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[st], 2 * ATOM);
+        tma_load_3d(smem + V_OFF + st * 32768, &tmV, &v_full[st], 0, j * BKV, b);
+        tma_load_3d(smem + V_OFF + st * 32768 + ATOM, &tmV, &v_full[st], 64, j * BKV, b);
+        armed[4 + st] = (int)ph;
+      }
     }
     if (*abort_flag) {
       int none = 0;
-      uint64_t* fb[5] = {q_full, &k_full[0], &k_full[1], &v_full[0], &v_full[1]};
-      for (int i = 0; i < 5; ++i)
+      uint64_t* fb[6] = {&q_full[0], &q_full[1], &k_full[0], &k_full[1], &v_full[0], &v_full[1]};
+      for (int i = 0; i < 6; ++i)
         if (armed[i] >= 0) mbar_wait_bounded(fb[i], (uint32_t)armed[i], &none, err, SITE_ATTN, timeout_ns / 8);
     }
-  } else if ((warp == 1 || warp == 3) && lane == 0) {
+  } else if ((warp == 1 || warp == 2) && lane == 0) {
     // ------------------------------------------------ MMA issuers
-    // Warp 1 issues the score products S(j) = Q K(j)^T, warp 3 the O += P(j)
-    // V(j) products.  An MMA issue holds its thread for about the MMA's run
-    // time, so one stream's waits and commits overlap the other's MMAs; a
-    // commit tracks the MMAs of its own thread (K is read only by the S
-    // products, V only by the PV products).  Descriptors are built once; a
-    // k-step or ring stage only moves the 14-bit start-address field (shared
-    // memory < 256 KB: no carry).
+    // Warp 1 issues tile 0's products, warp 2 tile 1's: per key tile j,
+    // S(j) = Q K(j)^T, then O += P(j) V(j) once the softmax warps have
+    // written P(j).  An MMA issue holds its thread for about the MMA's run
+    // time, so each issuer's waits overlap the other's MMAs; a commit tracks
+    // the MMAs of its own thread.  Tile 1 runs half a step behind tile 0:
+    // its S(j) is issued once tile 0's softmax warps have read their S(j),
+    // so that it computes while they do and their softmax and tile 1's take
+    // turns on the SM's schedulers instead of running at once.  Descriptors
+    // are built once; a k-step or ring stage only moves the 14-bit
+    // start-address field (shared memory < 256 KB: no carry).
+    const int x = warp == 1 ? 0 : 1;
     constexpr uint32_t idS = idesc_bf16_mn(false, false, BQ, BKV);
     constexpr uint32_t idPV = idesc_bf16_mn(false, true, BQ, HD);
     constexpr uint64_t kStage = 32768 >> 4;
     auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * ATOM + (kk & 3) * 32) >> 4); };
     auto moff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + Q_OFF + x * 32768), 16, 1024);
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), ATOM, 1024);  // MN-major
+    const uint32_t s_t = tmem + x * BKV, o_t = tmem + 256 + x * HD;
     bool ok = true, issued = false;
-    if (warp == 1) {
-      const uint64_t dQ = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
-      const uint64_t dK = sdesc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-      ok = sync.wait(q_full, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!sync.wait(&k_full[st], ph) || !sync.wait(&s_free[st], ph ^ 1u)) { ok = false; break; }
+    long g = 0, n = 0;  // key tiles streamed; this tile's (pair, key tile) steps
+    long n0 = 0;        // tile 0's steps before the current pair (tile 1's issuer)
+    for (int k = 0; ok; ++k) {
+      const long u = snake_item(cta, k, G, n_items);
+      if (u < 0) break;
+      const int nkx = key_tiles(u, x), nkv = key_tiles(u, 1), nk0 = key_tiles(u, 0);
+      if (!sync.wait(&q_full[x], k & 1)) { ok = false; break; }
+      for (int j = 0; j < nkx; ++j, ++g, ++n) {
+        const int st = (int)(g & 1);
+        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        // S overwrites the previous step's P: wait for the product that reads it.
+        if (!sync.wait(&k_full[st], ph) || (n > 0 && !sync.wait(&pv_done[x], (uint32_t)(n - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        // Tile 1: after tile 0's softmax has read S(j) (tile 0 is at most
+        // one step further on: its S(j + 2) needs the K stage that S(j) of
+        // this tile releases, so the two alternating barriers cannot alias).
+        if (x == 1 && j < nk0) {
+          const long m = n0 + j;
+          if (!sync.wait(&s0_read[m & 1], (uint32_t)(m >> 1) & 1u)) { ok = false; break; }
+        }
         tc_fence_after();
         const uint64_t bk = dK + st * kStage;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + st * BKV, dQ + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
-        umma_commit(&s_full[st]);
+          umma_bf16(s_t, dQ + koff(kk), bk + koff(kk), idS, kk > 0 ? 1u : 0u);
+        umma_commit(&s_full[x]);
         umma_commit(&k_empty[st]);
+        if (j == nkx - 1) umma_commit(&q_empty[x]);
         issued = true;
-      }
-    } else {
-      const uint64_t dV = sdesc_sw128(smem_u32(smem + V_OFF), ATOM, 1024);  // MN-major
-      for (int j = 0; ok && j < nkv; ++j) {
-        // O += P(j) V(j), P(j) read from tensor memory
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!sync.wait(&p_full[st], ph) || !sync.wait(&v_full[st], ph)) { ok = false; break; }
+        // P(j) written (and O rescaled; the first step of a pair also
+        // follows the softmax warps' read of the previous pair's O).
+        if (!sync.wait(&p_full[x], (uint32_t)n & 1u) || !sync.wait(&v_full[st], ph)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t bv = dV + st * kStage;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          umma_bf16_tmem_a(tmem + 256, tmem + 384 + st * 64 + kk * 8, bv + moff(kk), idPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[st]);
+          umma_bf16_tmem_a(o_t, s_t + kk * 8, bv + moff(kk), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[x]);
         umma_commit(&v_empty[st]);
-        issued = true;
       }
+      // Key tiles past this tile's last row: release their stages unread (once
+      // they have landed, so that the arrival counts toward their own phase).
+      for (int j = nkx; ok && j < nkv; ++j, ++g) {
+        const int st = (int)(g & 1);
+        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        if (!sync.wait(&k_full[st], ph)) { ok = false; break; }
+        mbar_arrive(&k_empty[st]);
+        if (!sync.wait(&v_full[st], ph)) { ok = false; break; }
+        mbar_arrive(&v_empty[st]);
+      }
+      n0 += nk0;
     }
     if ((!ok || *abort_flag) && issued) {
       int none = 0;
-      uint64_t* d = &drain[warp == 1 ? 0 : 1];
-      umma_commit(d);
-      mbar_wait_bounded(d, 0, &none, err, SITE_ATTN, timeout_ns / 8);
+      umma_commit(&drain[x]);
+      mbar_wait_bounded(&drain[x], 0, &none, err, SITE_ATTN, timeout_ns / 8);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 3) {
     // ------------------------------------------------ softmax / epilogue
-    // Warp 4 + 4 g + quarter owns packed rows 32 quarter .. 32 quarter + 31
-    // (its TMEM lanes) and key columns CW g .. CW g + CW - 1 of each tile; the
-    // NG column groups of a row exchange their maxima through shared memory.
-    // Four warps per scheduler hide each other's TMEM, barrier and SFU latency.
+    // Warps 3-6 serve tile 0, warps 7-10 tile 1; a warp reads TMEM lanes
+    // 32 (warp % 4) .. + 31, so it owns the tile's rows 32 quarter ..
+    // 32 quarter + 31 with quarter = warp % 4, one thread per row over all
+    // 128 keys of a key tile: a row's maximum needs no exchange.
+    const int x = (warp - 3) >> 2;
     const int quarter = warp & 3;
-    const int g = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;
-    const long r = r0 + row;
-    const bool valid = r < TH;
-    const int t = (int)(r / H);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_t = tmem + lane_off + x * BKV, o_t = tmem + lane_off + 256 + x * HD;
     const float sl2 = rsqrtf((float)HD) * kLog2e;
-    float* red = reinterpret_cast<float*>(smem + RED_OFF);
-    float* lsum = reinterpret_cast<float*>(smem + LSUM_OFF);
-    const int t0 = (int)(r0 / H);
-    const int tmax = min(t, T - 1);  // the last key this row sees
-    float m_run = -INFINITY, l_run = 0.f;  // l_run: this group's columns only
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!sync.wait(&s_full[st], ph)) { ok = false; break; }
-      tc_fence_after();
-      float s[CW];
-      tmem_ld_32cols(tmem + lane_off + st * BKV + g * CW, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-      const int key0 = j * BKV + g * CW;
-      float mx = -INFINITY;
+    long n = 0;  // this tile's (pair, key tile) steps
+    for (int k = 0; ok; ++k) {
+      const long u = snake_item(cta, k, G, n_items);
+      if (u < 0) break;
+      const int b = item_b(u);
+      const long rx0 = item_r0(u) + (long)x * BQ;
+      const long r = rx0 + row;
+      const bool valid = r < TH;
+      const int nkx = key_tiles(u, x);
+      const int tmax = (int)(min(r, TH - 1) / H);   // the last key this row sees
+      const int t0 = (int)(min(rx0, TH - 1) / H);   // the tile's first row's token
+      float m_run = -INFINITY, l_run = 0.f;  // in log2 units of the scaled scores
+      for (int j = 0; j < nkx; ++j, ++n) {
+        if (!sync.wait_warp(&s_full[x], (uint32_t)n & 1u)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t raw[4][32];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) {
-        s[i] *= sl2;
-        mx = fmaxf(mx, s[i]);
-      }
-      // Keys past a row's token (or past the sequence) occur only in tiles
-      // reaching beyond t0, the first row's token.
-      if (key0 + CW - 1 > t0) {
-        const int lim = tmax - key0;
-        mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          if (i > lim) s[i] = -INFINITY;
-          mx = fmaxf(mx, s[i]);
+        for (int c = 0; c < 4; ++c) tmem_ld_32cols_nowait(s_t + c * 32, raw[c]);
+        tmem_ld_wait();
+        if (x == 0) {  // lets tile 1's S(j) start (it writes other columns)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s0_read[n & 1]);
         }
-      }
-      // Exchange the groups' maxima (buffers alternate by tile parity, so a
-      // fast warp never overwrites values a slow one has yet to read).
-      float* rp = red + (j & 1) * NG * 128;
-      rp[g * 128 + row] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_full[j & 1]);
-      if (!sync.wait(&red_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+        float s[BKV];
 #pragma unroll
-      for (int q = 0; q < NG; ++q) mx = fmaxf(mx, rp[q * 128 + row]);
-      if (mx > m_run + 8.f) {
-        const float alpha = ex2(m_run - mx);  // 0 on the first tile
-        if (j > 0) {  // O is rescaled once the PV MMA of the previous tile is done
-          if (!sync.wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
+        for (int i = 0; i < BKV; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
+        // Keys past a row's token occur only in tiles reaching beyond t0.
+        if (j * BKV + BKV - 1 > t0) {
+          const int lim = tmax - j * BKV;
+#pragma unroll
+          for (int i = 0; i < BKV; ++i)
+            if (i > lim) s[i] = -INFINITY;
+        }
+        float m8[8];  // eight partial maxima: a short dependency chain
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+        for (int i = 8; i < BKV; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        mx *= sl2;
+        float alpha = 1.f;
+        if (mx > m_run + 8.f) {  // rescale only when the maximum grows by more than 2^8
+          alpha = ex2(m_run - mx);  // 0 on the first tile
+          l_run *= alpha;
+          m_run = mx;
+        }
+        const float nm = -m_run;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pk[BKV / 2];
+#pragma unroll
+        for (int i = 0; i < BKV; i += 2) {
+          float e0, e1;
+          fma2(e0, e1, s[i], s[i + 1], sl2, sl2, nm, nm);
+          const float p0 = ex2(e0), p1 = ex2(e1);
+          ls0 += p0;
+          ls1 += p1;
+          pk[i / 2] = pack2(p0, p1);
+        }
+        l_run += ls0 + ls1;
+        {
+          uint32_t (&h0)[32] = *reinterpret_cast<uint32_t(*)[32]>(pk);
+          uint32_t (&h1)[32] = *reinterpret_cast<uint32_t(*)[32]>(pk + 32);
+          pairs_to_tmem(s_t, h0);
+          pairs_to_tmem(s_t + 32, h1);
+        }
+        // O holds the products through P(j - 1) V(j - 1): S(j) was issued
+        // after that product completed, and s_full tracks both.  The TMEM
+        // load and store are warp-collective, so the whole warp takes the
+        // branch when any row rescales (the others multiply by 1).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = g * CW; c < (g + 1) * CW; c += 32) {
-            const uint32_t oc = tmem + lane_off + 256 + c;
+          for (int c = 0; c < HD; c += 32) {
             float v[32];
-            tmem_ld_32cols(oc, v);
+            tmem_ld_32cols(o_t + c, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st_32cols(oc, v);
+            tmem_st_32cols(o_t + c, v);
           }
         }
-        l_run *= alpha;
-        m_run = mx;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
       }
-      float ls = 0.f;
-      uint32_t pk[CW / 2];
-#pragma unroll
-      for (int i = 0; i < CW; i += 2) {
-        const float p0 = ex2(s[i] - m_run), p1 = ex2(s[i + 1] - m_run);
-        ls += p0 + p1;
-        pk[i / 2] = pack2(p0, p1);
-      }
-      l_run += ls;
-      // P(j) as bf16 pairs into P buffer st once the PV MMA of tile j - 2 has read it
-      if (j >= 2) {
-        if (!sync.wait(&pv_done[st], ((j - 2) >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
-      pairs16_to_tmem(tmem + lane_off + 384 + st * 64 + g * (CW / 2), pk);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
-    }
-    lsum[g * 128 + row] = l_run;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(lsum_full);
-    if (ok) ok = sync.wait(lsum_full, 0);
-    float l_tot = 0.f;
-#pragma unroll
-    for (int q = 0; q < NG; ++q) l_tot += lsum[q * 128 + row];
-    if (ok && sync.wait(&pv_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1)) {
+      if (!ok) break;
+      // The pair's last P V product done: O is final.  The next pair's first
+      // P V product (which overwrites O) follows this warp's next p_full
+      // arrival, after these loads.
+      if (!sync.wait_warp(&pv_done[x], (uint32_t)(n - 1) & 1u)) { ok = false; break; }
       tc_fence_after();
-      const float inv = 1.f / l_tot;
+      const float inv = 1.f / l_run;
       bf16* orow = o + ((long)b * TH + r) * HD;
 #pragma unroll 1
-      for (int c = g * CW; c < (g + 1) * CW; c += 32) {
+      for (int c = 0; c < HD; c += 32) {
         float v[32];
-        tmem_ld_32cols(tmem + lane_off + 256 + c, v);
+        tmem_ld_32cols(o_t + c, v);
         if (valid) store_bf16_32(orow + c, v, inv);
       }
-      if (valid && g == 0) lse[(long)b * TH + r] = (m_run + log2f(l_tot)) * kLn2;
+      if (valid) lse[(long)b * TH + r] = (m_run + log2f(l_run)) * kLn2;
+      tc_fence_before();
     }
   }
   tc_fence_before();
@@ -468,14 +548,6 @@ constexpr int kPrefetchAhead = 4;            // key tiles prefetched into L2 ahe
 static_assert(SMEM <= 232448, "dQ pass shared memory exceeds 227 KB");
 }  // namespace bdq
 
-// The k-th query tile (an index into the heaviest-first order: sequence
-// fastest, the last query tiles -- which see the most keys -- first) of CTA c
-// among G, or -1 past the end.  Round k covers tiles kG .. kG + G - 1, walked
-// forwards in even rounds and backwards in odd ones.
-__device__ __forceinline__ long dq_tile_of(int c, int k, int G, long n_tiles) {
-  const long u = (long)k * G + ((k & 1) ? G - 1 - c : c);
-  return u < n_tiles ? u : -1;
-}
 
 __global__ void __launch_bounds__(NT, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -565,7 +637,7 @@ __global__ void __launch_bounds__(NT, 1)
     long g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const long u = dq_tile_of(c, k, G, n_tiles);
+      const long u = snake_item(c, k, G, n_tiles);
       if (u < 0) break;
       const int b = tile_b(u);
       const int r0 = (int)tile_r0(u);
@@ -576,7 +648,7 @@ __global__ void __launch_bounds__(NT, 1)
       tma_load_3d(smem + DO_OFF, &tmDO, qd_full, 0, r0, b);
       tma_load_3d(smem + DO_OFF + ATOM, &tmDO, qd_full, 64, r0, b);
       armed_qd = k & 1;
-      const long un = dq_tile_of(c, k + 1, G, n_tiles);
+      const long un = snake_item(c, k + 1, G, n_tiles);
       if (un >= 0) {  // the next tile's rows into L2 while this one runs
         const int bn = tile_b(un), rn = (int)tile_r0(un);
         tma_prefetch_l2_3d(&tmQ, 0, rn, bn);
@@ -643,7 +715,7 @@ __global__ void __launch_bounds__(NT, 1)
       const uint64_t dQk = sdesc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t dOk = sdesc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
       for (int k = 0; ok; ++k) {
-        const long u = dq_tile_of(c, k, G, n_tiles);
+        const long u = snake_item(c, k, G, n_tiles);
         if (u < 0) break;
         const int nkv = tile_nkv(u);
         if (!sync.wait(qd_full, (uint32_t)k & 1u)) { ok = false; break; }
@@ -680,7 +752,7 @@ __global__ void __launch_bounds__(NT, 1)
     } else {
       const uint64_t dKm = sdesc_sw128(smem_u32(smem + K_OFF), ATOM, 1024);  // MN-major
       for (int k = 0; ok; ++k) {
-        const long u = dq_tile_of(c, k, G, n_tiles);
+        const long u = snake_item(c, k, G, n_tiles);
         if (u < 0) break;
         const int nkv = tile_nkv(u);
         for (int j = 0; j < nkv; ++j, ++g) {
@@ -724,7 +796,7 @@ __global__ void __launch_bounds__(NT, 1)
       d = v ? delta[grow] : 0.f;
       l2 = v ? lse[grow] * kLog2e : 0.f;
     };
-    long u = dq_tile_of(c, 0, G, n_tiles);
+    long u = snake_item(c, 0, G, n_tiles);
     float lse2 = 0.f, dl = 0.f;
     if (u >= 0) row_data(u, lse2, dl);
     for (int k = 0; ok && u >= 0; ++k) {
@@ -734,7 +806,7 @@ __global__ void __launch_bounds__(NT, 1)
       const bool valid = r < TH;
       const int t = (int)(r / H);
       const int nkv = tile_nkv(u);
-      const long un = dq_tile_of(c, k + 1, G, n_tiles);
+      const long un = snake_item(c, k + 1, G, n_tiles);
       float lse2_n = 0.f, dl_n = 0.f;
       if (un >= 0) row_data(un, lse2_n, dl_n);
       // Rows of this tile hold tokens t0 .. ; a key tile needs the mask only
@@ -742,7 +814,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int t0 = (int)(r0 / H);
       const bool rows_ragged = r0 + BQ > TH;
       for (int j = 0; j < nkv; ++j, ++g) {
-        if (!sync.wait(s_full, (uint32_t)g & 1u)) { ok = false; break; }
+        if (!sync.wait_warp(s_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
         float s[64], dp[64];
         {
@@ -769,7 +841,7 @@ __global__ void __launch_bounds__(NT, 1)
           for (int i = 0; i < 64; ++i)
             if (i > lim) s[i] = 0.f;
         }
-        if (!sync.wait(dp_full, (uint32_t)g & 1u)) { ok = false; break; }
+        if (!sync.wait_warp(dp_full, (uint32_t)g & 1u)) { ok = false; break; }
         tc_fence_after();
         {
           uint32_t r2_[32], r3_[32];
@@ -793,7 +865,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = pack2(s[2 * i], s[2 * i + 1]);
         if (g > 1) {  // the dQ MMA of pair g - 2 has read this dS buffer
-          if (!sync.wait(&dq_done[db], (uint32_t)((g >> 1) - 1) & 1u)) { ok = false; break; }
+          if (!sync.wait_warp(&dq_done[db], (uint32_t)((g >> 1) - 1) & 1u)) { ok = false; break; }
           tc_fence_after();
         }
         pairs_to_tmem(tmem + lane_off + 384 + db * 64 + half * 32, pk);
@@ -803,7 +875,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       if (!ok) break;
       // dQ MMAs complete in issue order: the tile's last one done means all are.
-      if (!sync.wait(dq_full, (uint32_t)k & 1u)) { ok = false; break; }
+      if (!sync.wait_warp(dq_full, (uint32_t)k & 1u)) { ok = false; break; }
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       bf16* qrow = dq + ((long)b * T + t) * ldq + (long)(r % H) * HD;
@@ -1110,7 +1182,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int st = i & 1;
       // packed rows rowbase .. rowbase + 63 are this thread's query columns
       const long rowbase = (rt0 + i) * BQ + half * 64;
-      if (!sync.wait(sc_full, 0) || !sync.wait(&info_full[st], (i >> 1) & 1)) {
+      if (!sync.wait_warp(sc_full, 0) || !sync.wait_warp(&info_full[st], (i >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -1151,14 +1223,14 @@ __global__ void __launch_bounds__(NT, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) pk[j] = pack2(x[2 * j], x[2 * j + 1]);
-      if (i > 0 && !sync.wait(pt_free, (i - 1) & 1)) { ok = false; break; }
+      if (i > 0 && !sync.wait_warp(pt_free, (i - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       pairs_to_tmem(tmem + lane_off + 384 + half * 32, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
       // dS^T = P^T (dP^T - delta), with P^T as stored (bf16)
-      if (!sync.wait(sc_full, 1)) { ok = false; break; }
+      if (!sync.wait_warp(sc_full, 1)) { ok = false; break; }
       tc_fence_after();
       {
         uint32_t r0_[32], r1_[32];
@@ -1189,14 +1261,14 @@ __global__ void __launch_bounds__(NT, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&info_free[st]);
-      if (i > 0 && !sync.wait(dst_free, (i - 1) & 1)) { ok = false; break; }
+      if (i > 0 && !sync.wait_warp(dst_free, (i - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       pairs_to_tmem(tmem + lane_off + 448 + half * 32, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-    if (ok && n_rt > 0 && sync.wait(dst_free, (n_rt - 1) & 1)) {
+    if (ok && n_rt > 0 && sync.wait_warp(dst_free, (n_rt - 1) & 1)) {
       tc_fence_after();
       const float scale = rsqrtf((float)HD);
       const long tok = (long)b * T + key;
@@ -1247,9 +1319,10 @@ cudaError_t attention_fwd_tc(int B, int T, int H, const void* q, const void* k, 
   if (!map3(&mq, q, TH, B, fwd::BQ) || !map3(&mk, k, T, B, fwd::BKV) ||
       !map3(&mv, v, T, B, fwd::BKV))
     return cudaErrorInvalidValue;
-  dim3 grid(B, (unsigned)((TH + fwd::BQ - 1) / fwd::BQ));
-  attn_fwd_tc_kernel<<<grid, fwd::NTF, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, T, H,
-                                                          ctx.err, ctx.timeout_ns);
+  const long items = (long)B * ((TH + 2 * fwd::BQ - 1) / (2 * fwd::BQ));
+  const unsigned grid = (unsigned)std::min<long>(items, std::max(ctx.num_sms, 1));
+  attn_fwd_tc_kernel<<<grid, fwd::NTF, fwd::SMEM, ctx.stream>>>(mq, mk, mv, (nc::bf16*)o, lse, B, T,
+                                                          H, ctx.err, ctx.timeout_ns);
   return launched(1);
 }
 

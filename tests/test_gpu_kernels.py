@@ -189,3 +189,52 @@ def test_attention_fwd_bwd_matches_oracle(dtype, h, B, T, H):
             assert cos > 0.999 and rel < 2e-2, (name, cos, rel)
         else:
             assert rel < 2e-5, (name, rel)
+
+
+def test_attention_running_maximum_grows_every_key_tile():
+    """Scores that rise along the keys (k_t = c (t / T) u + noise, q = 16 u +
+    noise for a unit vector u): from one 128-key tile to the next a row's
+    maximum grows by ~40 nats (~58 in log2 units), far past the 2^8 margin
+    within which the online softmax keeps its running maximum, so the
+    forward rescales its output accumulator on every key tile.  Output,
+    log-sum-exp, dK and dV against the oracle.  dQ is left out: with P nearly
+    one-hot, dP - delta is a difference of nearly equal terms, weighted by
+    keys of norm ~141, and the bf16 rounding of the stored output that enters
+    delta = rowsum(O * dO) moves dQ by ~5 % on its own (an fp64 replay of the
+    method with only that rounding gives cos 0.9989): a conditioning property
+    of this input, not of the running maximum tested here."""
+    B, T, H, h = 2, 640, 3, 128
+    rng = np.random.default_rng(640)
+    u = rng.standard_normal(h)
+    u /= np.linalg.norm(u)
+    c = 200.0 * np.sqrt(h) / 16.0                 # last key's score ~200 nats
+    q = 16.0 * u + 0.3 * rng.standard_normal((B, T, H, h))
+    k = c * (np.arange(T) / T)[None, :, None] * u + 0.3 * rng.standard_normal((B, T, h))
+    v = rng.standard_normal((B, T, h))
+    do = rng.standard_normal((B, T, H, h))
+    rt = lambda a: torch.from_numpy(a).to(torch.bfloat16).double().numpy()  # noqa: E731
+    q, k, v, do = rt(q), rt(k), rt(v), rt(do)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).cuda()  # noqa: E731
+    qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)
+    o = torch.zeros_like(qd)
+    lse = torch.zeros(B, T, H, device="cuda")
+    nc.attention_fwd(nc.NC_BF16, B, T, H, h, qd, kd, vd, o, lse)
+    W = (H + 2) * h
+    dqkv = torch.full((B * T, W), 7.0, dtype=torch.bfloat16, device="cuda")
+    nc.attention_bwd(nc.NC_BF16, B, T, H, h, qd, kd, vd, o, lse, dod, dqkv[:, :H * h], W,
+                     dqkv[:, H * h:H * h + h], W, dqkv[:, H * h + h:], W)
+    torch.cuda.synchronize()
+    s = np.einsum("bthd,bjd->bhtj", q, k) / np.sqrt(h)
+    s = np.where(np.triu(np.ones((T, T), bool), 1)[None, None], -np.inf, s)
+    m = s.max(-1, keepdims=True)
+    assert float(m[..., -1, 0].min()) > 150.0      # the construction did what it says
+    lse_ref = (m + np.log(np.exp(s - m).sum(-1, keepdims=True)))[..., 0].transpose(0, 2, 1)
+    np.testing.assert_allclose(lse.double().cpu().numpy(), lse_ref, rtol=1e-4, atol=2e-2)
+    _, dk_ref, dv_ref = oracle.attention_bwd(do, q, k, v)
+    got = {"o": o.double().cpu().numpy(),
+           "dk": dqkv[:, H * h:H * h + h].double().cpu().numpy().reshape(B, T, h),
+           "dv": dqkv[:, H * h + h:].double().cpu().numpy().reshape(B, T, h)}
+    ref = {"o": oracle.attention(q, k, v), "dk": dk_ref, "dv": dv_ref}
+    for name in ref:
+        cos, rel = grad_metrics(ref[name], got[name])
+        assert cos > 0.999 and rel < 2e-2, (name, cos, rel)

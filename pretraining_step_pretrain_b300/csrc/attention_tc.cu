@@ -158,6 +158,36 @@ __device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// a += b on both halves of a packed fp32 pair.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, b;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// 64 bf16 pairs of this thread's row into its TMEM lane (64 columns), one
+// wait for both halves.
+__device__ __forceinline__ void pairs64_to_tmem(uint32_t taddr, const uint32_t (&p)[64]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t* q = p + 32 * h;
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr + 32 * h),
+        "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]),
+        "r"(q[8]), "r"(q[9]), "r"(q[10]), "r"(q[11]), "r"(q[12]), "r"(q[13]), "r"(q[14]),
+        "r"(q[15]), "r"(q[16]), "r"(q[17]), "r"(q[18]), "r"(q[19]), "r"(q[20]), "r"(q[21]),
+        "r"(q[22]), "r"(q[23]), "r"(q[24]), "r"(q[25]), "r"(q[26]), "r"(q[27]), "r"(q[28]),
+        "r"(q[29]), "r"(q[30]), "r"(q[31])
+        : "memory");
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Work item k of CTA c among G persistent CTAs: round k takes items k G ..
 // k G + G - 1, forwards in even rounds and backwards in odd ones.
 __device__ __forceinline__ long snake_item(int c, int k, int G, long n_items) {
@@ -433,17 +463,11 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
           float e0, e1;
           fma2(e0, e1, s[i], s[i + 1], sl2, sl2, nm, nm);
           const float p0 = ex2(e0), p1 = ex2(e1);
-          ls0 += p0;
-          ls1 += p1;
+          add2(ls0, ls1, p0, p1);
           pk[i / 2] = pack2(p0, p1);
         }
         l_run += ls0 + ls1;
-        {
-          uint32_t (&h0)[32] = *reinterpret_cast<uint32_t(*)[32]>(pk);
-          uint32_t (&h1)[32] = *reinterpret_cast<uint32_t(*)[32]>(pk + 32);
-          pairs_to_tmem(s_t, h0);
-          pairs_to_tmem(s_t + 32, h1);
-        }
+        pairs64_to_tmem(s_t, pk);
         // O holds the products through P(j - 1) V(j - 1): S(j) was issued
         // after that product completed, and s_full tracks both.  The TMEM
         // load and store are warp-collective, so the whole warp takes the

@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
   uint64_t* p_full = bars + 14;   // [2] by tile, one arrival per softmax warp
   uint64_t* pv_done = bars + 16;  // [2] by tile
   uint64_t* drain = bars + 18;    // [2] by tile (its MMA issuer)
-  uint64_t* s0_read = bars + 20;  // [2] by tile 0's step parity: its softmax has read S
+  uint64_t* s0_read = bars + 20;  // [2] by tile 0's step parity: its softmax has S's row maxima
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
     // written P(j).  An MMA issue holds its thread for about the MMA's run
     // time, so each issuer's waits overlap the other's MMAs; a commit tracks
     // the MMAs of its own thread.  Tile 1 runs half a step behind tile 0:
-    // its S(j) is issued once tile 0's softmax warps have read their S(j),
+    // its S(j) is issued once tile 0's softmax warps have their S(j) row maxima,
     // so that it computes while they do and their softmax and tile 1's take
     // turns on the SM's schedulers instead of running at once.  Descriptors
     // are built once; a k-step or ring stage only moves the 14-bit
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
           ok = false;
           break;
         }
-        // Tile 1: after tile 0's softmax has read S(j) (tile 0 is at most
+        // Tile 1: after tile 0's softmax has S(j)'s row maxima (tile 0 is at most
         // one step further on: its S(j + 2) needs the K stage that S(j) of
         // this tile releases, so the two alternating barriers cannot alias).
         if (x == 1 && j < nk0) {
@@ -427,10 +427,6 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_32cols_nowait(s_t + c * 32, raw[c]);
         tmem_ld_wait();
-        if (x == 0) {  // lets tile 1's S(j) start (it writes other columns)
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s0_read[n & 1]);
-        }
         float s[BKV];
 #pragma unroll
         for (int i = 0; i < BKV; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
@@ -448,6 +444,14 @@ __global__ void __launch_bounds__(fwd::NTF, 1)
         for (int i = 8; i < BKV; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
         float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // Tile 1's S(j) may start now (it writes other columns): issued here,
+        // its product lands about when this warpgroup's exponentials end
+        // (measured against releasing it right after the load, or after P is
+        // stored: 2 % faster, and 5 % faster).
+        if (x == 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s0_read[n & 1]);
+        }
         mx *= sl2;
         float alpha = 1.f;
         if (mx > m_run + 8.f) {  // rescale only when the maximum grows by more than 2^8

@@ -100,18 +100,6 @@ __device__ __forceinline__ void pairs_to_tmem(uint32_t taddr, const uint32_t (&p
   tmem_st_32cols(taddr, v);
 }
 
-// 16 bf16 pairs of this thread's row into its TMEM lane (16 columns).
-__device__ __forceinline__ void pairs16_to_tmem(uint32_t taddr, const uint32_t (&p)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]),
-      "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]),
-      "r"(p[15])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 struct CtaSync {
   volatile int* abort_flag;
   int* err;
